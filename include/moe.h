@@ -1,0 +1,304 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) single-GPU MoE dispatch -> grouped
+ * expert MLP -> combine library.
+ *
+ * The four calls of one MoE layer forward, in stream order:
+ *
+ *   moe_preprocess         routing map -> per-expert counts, padded offsets,
+ *                          stable row map, overflow flag (all on the device)
+ *   moe_dispatch_permute   token rows (+ probabilities, + FP8 / NVFP4 scales)
+ *                          -> expert-grouped rows in a caller-owned buffer
+ *   moe_grouped_mlp        FC1 -> SwiGLU -> FC2 per expert, FC2 rows written
+ *                          into a caller-owned buffer
+ *   moe_combine_unpermute  expert rows -> token order, top-k probability-
+ *                          weighted sum
+ *
+ * Sources, by page title and section:
+ *   [REUSE-BUF] Megatron-LM PR #6800 "Reuse caller-owned HybridEP dispatch and
+ *               expert output buffers" (Summary; Configuration; Known
+ *               limitations): dispatch and grouped FC2 write into persistent
+ *               caller-owned rings; the final consumer releases a slot; early
+ *               reuse and double release fail explicitly; a static output bound
+ *               is required.
+ *   [ALLGATHER] DeepEP PR #716 "perf: reuse HybridEP routing allgather buffer"
+ *               (Memory impact; Testing): sparse Boolean tokens x experts and
+ *               dense int16 tokens x topk routing maps; padding multiple;
+ *               dispatch with permutation and combine with unpermutation, with
+ *               and without probabilities; bitwise-identical dispatched rows.
+ *   [SYNC-FREE] NeMo Automodel PR #3931 "perf(moe): sync-free HybridEP dispatch
+ *               (capacity mode, equal token counts)" (What does this PR do?;
+ *               Validation): non-blocking dispatch sized by a host integer
+ *               capacity = ceil(rows x factor), 4-aligned; real counts stay on
+ *               the device; an overflow flag in the handle replaces the host
+ *               sync; truncation past the capacity is silent.
+ *   [ELASTIC]   Megatron-LM PR #4632 "moe: add DeepEP V2 ElasticBuffer support
+ *               to MoE flex dispatcher" (Motivation): the per-expert counts live
+ *               on the dispatch handle; the layout is inferred from the top-k ids.
+ *   [MEGAMOE]   TensorRT-LLM PR #16190 "Update CuTeDSL MegaMoE kernels" (commit
+ *               list): NVFP4 expert weights w3_w1 / w2 with block scales,
+ *               weight_scale_2 and input_scale; zero-token launches keep a
+ *               non-empty grid; int64 offsets into large pools; zero only the
+ *               leading workspace bytes that need it.
+ *
+ * Conventions (all calls):
+ *   - Every device buffer is owned by the caller.  The library never allocates
+ *     or frees device memory and never synchronises the host with the device.
+ *     All work is enqueued on the given CUDA stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream), so the four calls can be
+ *     captured into one CUDA graph and replayed.
+ *   - Arguments are validated on the host before anything is enqueued; a bad
+ *     argument returns MOE_ERR_INVALID_ARG and enqueues nothing.
+ *   - Capacity overflow is not an error status: it is the device int32 flag
+ *     handle->overflow, which the caller reads when it chooses to.
+ *   - Device-side anomalies (malformed routing, a bounded wait that ran out)
+ *     set bits of the device int32 handle->status; no kernel ever traps.
+ *   - Row and byte offsets are computed in 64-bit integers.
+ *   - Device pointers to rows must be 16-byte aligned; H must be a multiple of
+ *     128 (so every row is a whole number of 16-byte vectors and 128-element
+ *     FP8 scale blocks).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* bad pointer, shape, alignment or enum */
+  MOE_ERR_UNSUPPORTED = 2,          /* dtype / shape combination not built, or no sm_103 device */
+  MOE_ERR_CUDA = 3,                 /* a CUDA call failed; see moe_last_cuda_error() */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace smaller than the *_workspace_size query */
+  MOE_ERR_RING_EARLY_REUSE = 5,     /* ring slot acquired again before its release */
+  MOE_ERR_RING_DOUBLE_RELEASE = 6   /* ring slot released while not held */
+} moe_status;
+
+/* Routing map layouts ([ALLGATHER], Memory impact). */
+enum {
+  MOE_ROUTING_DENSE_I16 = 0,   /* int16 topk_idx [T][K]; -1 = no route in that slot;
+                                  probs (optional) float [T][K] */
+  MOE_ROUTING_SPARSE_BOOL = 1  /* uint8 map [T][E], nonzero = routed; slot k of a token
+                                  is its k-th routed expert in ascending expert order;
+                                  probs (optional) float [T][E] */
+};
+
+/* Element formats of dispatched rows and expert weights. */
+enum {
+  MOE_DTYPE_BF16 = 0,            /* bf16 rows */
+  MOE_DTYPE_FP8_E4M3_B128 = 1,   /* E4M3 codes + one fp32 scale per 128 consecutive
+                                    elements of a row (activations) or per 128x128
+                                    block (weights) */
+  MOE_DTYPE_BF16_TO_FP8 = 2,     /* dispatch only: bf16 input quantized to
+                                    MOE_DTYPE_FP8_E4M3_B128 on the way */
+  MOE_DTYPE_NVFP4 = 3,           /* packed E2M1 (2 per byte, even element in the low
+                                    nibble) + one E4M3 scale per 16 consecutive
+                                    elements + one fp32 global scale */
+  MOE_DTYPE_BF16_TO_NVFP4 = 4    /* dispatch only: bf16 input quantized to NVFP4 */
+};
+
+/* Bits of the device status word handle->status. */
+#define MOE_DEV_ERR_BAD_EXPERT 1      /* a dense id outside [-1, E): treated as no route */
+#define MOE_DEV_ERR_TOO_MANY_ROUTES 2 /* a sparse row with more than K routed experts:
+                                         the extra ones are ignored */
+#define MOE_DEV_ERR_TIMEOUT 4         /* a bounded inter-CTA wait gave up; outputs of
+                                         that call are not valid */
+
+typedef struct moe_shape {
+  int64_t T; /* tokens (>= 0) */
+  int64_t H; /* hidden size (multiple of 128) */
+  int64_t E; /* experts (1..1024) */
+  int64_t K; /* routes per token (1..128, K <= E) */
+  int64_t I; /* SwiGLU intermediate size (multiple of 128; 0 when no MLP is run) */
+} moe_shape;
+
+typedef struct moe_layout {
+  int64_t pad_multiple; /* m: each expert's segment is padded to a multiple of m (>= 1) */
+  int64_t capacity;     /* cap: rows of the dispatch / expert-output buffers (>= 0).
+                           Routes whose destination row reaches cap are dropped. */
+} moe_layout;
+
+typedef struct moe_routing {
+  int32_t format;     /* MOE_ROUTING_* */
+  const void* map;    /* device pointer, layout per format */
+  const float* probs; /* device pointer or NULL */
+} moe_routing;
+
+/* Device arrays written by moe_preprocess and read by the other calls (the
+ * "handle" of [SYNC-FREE] / [ELASTIC]).  All caller-owned device memory. */
+typedef struct moe_handle_dev {
+  int32_t* tokens_per_expert; /* [E]   real routed count per expert (never clamped) */
+  int32_t* padded_offsets;    /* [E+1] offsets[e] = sum_{e'<e} ceil(count[e']/m)*m */
+  int32_t* row_of;            /* [T*K] destination row of route (t,k), or -1 */
+  int32_t* token_of;          /* [cap] source token of each row < min(offsets[E],cap);
+                                       -1 for pad rows; rows beyond are not written */
+  int32_t* slot_of;           /* [cap] route slot k of each such row; -1 for pad rows */
+  int32_t* total_rows;        /* [1]   offsets[E] (unclamped) */
+  int32_t* overflow;          /* [1]   1 when offsets[E] > cap, else 0 */
+  int32_t* status;            /* [1]   MOE_DEV_ERR_* bits of the last preprocess */
+} moe_handle_dev;
+
+/* ---------------------------------------------------------------- helpers */
+
+/* Capacity rule of [SYNC-FREE], What does this PR do?: ceil(rows x factor)
+ * rounded up to a multiple of align (the pages use 4).  rows >= 0, factor > 0,
+ * align >= 1.  Host only. */
+MOE_API moe_status moe_capacity(int64_t rows, double factor, int64_t align, int64_t* capacity_out);
+
+/* Bytes of a routing map ([ALLGATHER], Memory impact): T*E for the sparse
+ * Boolean layout, T*K*2 for dense int16 ids.  Host only. */
+MOE_API moe_status moe_routing_map_bytes(int32_t format, int64_t T, int64_t E, int64_t K, size_t* bytes_out);
+
+/* Message of the last CUDA error seen by this thread's library calls. */
+MOE_API const char* moe_last_cuda_error(void);
+MOE_API const char* moe_status_string(moe_status s);
+
+/* ------------------------------------------------------------- preprocess */
+
+/* Device workspace bytes moe_preprocess needs for this shape (host only). */
+MOE_API moe_status moe_preprocess_workspace_size(const moe_shape* shape, size_t* bytes_out);
+
+/* Metadata preprocessing ([ALLGATHER], Summary: the routing map is consumed by
+ * metadata preprocessing on the same stream before dispatch; [SYNC-FREE]).
+ * Computes, on the device, every array of *handle:
+ *   tokens_per_expert, padded_offsets, total_rows, overflow: as documented in
+ *   moe_handle_dev;
+ *   row_of[t*K+k] = padded_offsets[e] + (number of routes (t',k') to the same
+ *   expert e that come before (t,k) in (token, slot) order), i.e. a stable sort
+ *   of the routes by expert, or -1 when that destination is >= capacity (the
+ *   route is dropped) or the slot has no route.
+ * routing: map (and probs, unused here) on the device.  workspace: device
+ * memory of at least moe_preprocess_workspace_size bytes, 16-byte aligned; its
+ * contents need no initialisation and are scratch between calls.
+ * Runs 2 memsets and 2 kernels on `stream`; no host sync. */
+MOE_API moe_status moe_preprocess(const moe_routing* routing, const moe_shape* shape, const moe_layout* layout,
+                          const moe_handle_dev* handle, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* --------------------------------------------------------------- dispatch */
+
+/* dispatch_with_permute ([REUSE-BUF], Summary; [ALLGATHER], Testing): for every
+ * route (t,k) with r = row_of[t*K+k] >= 0:
+ *   out_tokens[r] = x[t] (bitwise for BF16 / FP8 input; quantized on the way for
+ *                  BF16_TO_FP8 / BF16_TO_NVFP4),
+ *   out_scales[r] = that row's scales (FP8: fp32 [H/128]; NVFP4: E4M3 codes [H/16]),
+ *   out_probs[r]  = the route's probability (when out_probs and routing->probs
+ *                   are both non-NULL).
+ * Pad rows [offsets[e]+count[e], offsets[e+1]) below the capacity are written
+ * with zeros (tokens, scales and probability).  Rows at or beyond
+ * min(offsets[E], cap) are not touched.
+ * in_dtype: MOE_DTYPE_BF16 (x bf16 [T][H]), MOE_DTYPE_FP8_E4M3_B128 (x codes
+ * [T][H] + x_scales fp32 [T][H/128]), MOE_DTYPE_BF16_TO_FP8 (x bf16; output
+ * codes + fp32 scales; scale = amax/448 per 128 elements, 1 for an all-zero
+ * block, code = E4M3(x / scale) rounded to nearest even, saturating),
+ * MOE_DTYPE_BF16_TO_NVFP4 (x bf16; output packed E2M1 [H/2] + E4M3 scale codes
+ * [H/16] with the fp32 global scale *nvfp4_global (device pointer, passed in
+ * x_scales): block scale = E4M3(amax / (6 * global)), code = E2M1(x / (block *
+ * global))).
+ * out_tokens: device [cap][row bytes]; out_scales: device or NULL (required for
+ * FP8 / NVFP4 outputs); out_probs: device float [cap] or NULL. */
+MOE_API moe_status moe_dispatch_permute(const moe_handle_dev* handle, const moe_shape* shape,
+                                const moe_layout* layout, int32_t in_dtype, const void* x,
+                                const void* x_scales, const moe_routing* routing, void* out_tokens,
+                                float* out_probs, void* out_scales, void* stream);
+
+/* ---------------------------------------------------------------- combine */
+
+/* combine with unpermutation ([ALLGATHER], Testing; [MEGAMOE], TopkReduce):
+ *   y[t] = bf16( sum over k ascending with r = row_of[t*K+k] >= 0 of
+ *                w(r) * expert_out[r] )
+ * with fp32 accumulation, w(r) = perm_probs[r] or 1 when perm_probs is NULL.
+ * A token whose routes were all dropped gets zeros.
+ * expert_out: device bf16 [cap][H]; perm_probs: device float [cap] or NULL;
+ * y: device bf16 [T][H]. */
+MOE_API moe_status moe_combine_unpermute(const moe_handle_dev* handle, const moe_shape* shape,
+                                 const moe_layout* layout, const void* expert_out,
+                                 const float* perm_probs, void* y, void* stream);
+
+/* ------------------------------------------------------------ grouped MLP */
+
+/* Device workspace bytes of moe_grouped_mlp (the intermediate activation
+ * [cap][I] in the FC2 input format, plus its scales). */
+MOE_API moe_status moe_grouped_mlp_workspace_size(const moe_shape* shape, const moe_layout* layout,
+                                          int32_t w_dtype, size_t* bytes_out);
+
+/* NVFP4 global scales ([MEGAMOE]: weight_scale_2, input_scale; alpha derives
+ * from both).  All device pointers. */
+typedef struct moe_nvfp4_globals {
+  const float* fc1_input_scale; /* [1] global scale of the dispatched rows */
+  const float* fc2_input_scale; /* [1] global scale the intermediate is encoded with */
+  const float* w13_scale_2;     /* [E] per-expert global scale of w3_w1 */
+  const float* w2_scale_2;      /* [E] per-expert global scale of w2 */
+} moe_nvfp4_globals;
+
+/* Grouped SwiGLU expert MLP ([REUSE-BUF], Summary: fused grouped MLP writes FC2
+ * into a caller buffer).  For every expert e and every row r of its padded
+ * segment [offsets[e], offsets[e+1]) below the capacity:
+ *   up   = Y[r] . w13[e][0:I]^T,   gate = Y[r] . w13[e][I:2I]^T   (fp32 accumulate)
+ *   act  = silu(gate) * up, stored in the FC2 input format (bf16, FP8 with
+ *          1x128 fp32 scales, or NVFP4 with the fc2 input global scale)
+ *   out_fc2[r] = bf16( act . w2[e]^T )
+ * (w3_w1 order: rows 0..I-1 are w3 = up, rows I..2I-1 are w1 = gate.)  Pad rows
+ * hold zero input and so produce zero output.  Rows at or beyond
+ * min(offsets[E], cap) are not touched.
+ * w_dtype: MOE_DTYPE_BF16 (perm_tokens bf16 [cap][H]; w13 bf16 [E][2I][H]; w2
+ *   bf16 [E][H][I]);
+ *   MOE_DTYPE_FP8_E4M3_B128 (perm_tokens codes [cap][H] + perm_scales fp32
+ *   [cap][H/128]; w13 codes [E][2I][H] + w13_scales fp32 [E][2I/128][H/128]; w2
+ *   codes [E][H][I] + w2_scales fp32 [E][H/128][I/128]);
+ *   MOE_DTYPE_NVFP4 (perm_tokens packed [cap][H/2] + perm_scales E4M3 [cap][H/16];
+ *   w13 packed [E][2I][H/2] + E4M3 [E][2I][H/16]; w2 packed [E][H][I/2] + E4M3
+ *   [E][H][I/16]; globals required).
+ * workspace: device, >= moe_grouped_mlp_workspace_size bytes, 1024-byte aligned.
+ * out_fc2: device bf16 [cap][H]. */
+MOE_API moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
+                           int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
+                           const void* w13, const void* w13_scales, const void* w2,
+                           const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
+                           size_t workspace_bytes, void* out_fc2, void* stream);
+
+/* ------------------------------------------------- weight / row quantizers */
+
+/* bf16 [G][N][Kd] -> E4M3 codes [G][N][Kd] + fp32 scales [G][N/128][Kd/128],
+ * one scale per 128x128 block: scale = amax/448 (1 for an all-zero block),
+ * code = E4M3(w / scale), nearest even, saturating.  N, Kd multiples of 128.
+ * A one-time weight preparation step, not part of the per-layer path. */
+MOE_API moe_status moe_quantize_fp8_blocks(const void* w, int64_t G, int64_t N, int64_t Kd, void* codes,
+                                   float* scales, void* stream);
+
+/* bf16 [R][Kd] -> NVFP4 packed [R][Kd/2] + E4M3 scale codes [R][Kd/16] with
+ * the fp32 global scale *global (device pointer):
+ * block scale = E4M3(amax/(6*global)), code = E2M1(x/(block*global)). */
+MOE_API moe_status moe_quantize_nvfp4_rows(const void* x, int64_t R, int64_t Kd, const float* global,
+                                   void* packed, void* scales, void* stream);
+
+/* ------------------------------------------------------------ buffer ring */
+
+/* Host-side ring of N caller-owned output slots ([REUSE-BUF], Summary and
+ * Known limitations): the producer acquires the next slot in round-robin
+ * order; the final consumer releases it on its stream.  With events enabled,
+ * acquire makes `stream` wait (device-side, no host sync) on the event recorded
+ * by the slot's last release.  Acquiring a slot that is still held returns
+ * MOE_ERR_RING_EARLY_REUSE; releasing a slot that is not held returns
+ * MOE_ERR_RING_DOUBLE_RELEASE; neither changes the ring.  The ring only tracks
+ * slot indices: the caller maps a slot index to its own buffers. */
+typedef struct moe_ring moe_ring;
+MOE_API moe_status moe_ring_create(int32_t n_slots, int32_t use_events, moe_ring** ring_out);
+MOE_API moe_status moe_ring_acquire(moe_ring* ring, void* stream, int32_t* slot_out);
+MOE_API moe_status moe_ring_release(moe_ring* ring, int32_t slot, void* stream);
+MOE_API moe_status moe_ring_destroy(moe_ring* ring);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

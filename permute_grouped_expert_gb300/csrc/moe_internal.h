@@ -1,0 +1,64 @@
+// moe_internal.h -- launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Preprocess tiling: tokens per tile so that one tile holds at most this many routes.
+constexpr int kPreMaxEntries = 4096;
+constexpr int kPreThreads = 256;
+constexpr int kPreWarps = kPreThreads / 32;
+
+inline int64_t pre_tokens_per_tile(int64_t K) {
+  int64_t t = kPreMaxEntries / K;
+  return t < 1 ? 1 : t;
+}
+inline int64_t pre_num_tiles(int64_t T, int64_t K) {
+  int64_t tpt = pre_tokens_per_tile(K);
+  int64_t n = (T + tpt - 1) / tpt;
+  return n < 1 ? 1 : n;  // a zero-token call still runs one (empty) tile
+}
+
+struct PreWorkspace {
+  int32_t* tile_counter;       // [1]
+  uint64_t* lookback;          // [num_tiles][E]
+  int16_t* route_expert;       // [T*K]
+  size_t memset_bytes;         // leading bytes to clear per call (counter + lookback)
+};
+
+size_t preprocess_workspace_bytes(int64_t T, int64_t E, int64_t K);
+PreWorkspace preprocess_workspace_carve(void* ws, int64_t T, int64_t E, int64_t K);
+
+cudaError_t launch_preprocess(const moe_routing& r, const moe_shape& s, const moe_layout& l,
+                              const moe_handle_dev& h, const PreWorkspace& ws, cudaStream_t st);
+
+cudaError_t launch_dispatch(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                            int32_t in_dtype, const void* x, const void* x_scales,
+                            const moe_routing& r, void* out_tokens, float* out_probs,
+                            void* out_scales, cudaStream_t st);
+
+cudaError_t launch_combine(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                           const void* expert_out, const float* perm_probs, void* y,
+                           cudaStream_t st);
+
+cudaError_t launch_quantize_fp8_blocks(const void* w, int64_t G, int64_t N, int64_t Kd, void* codes,
+                                       float* scales, cudaStream_t st);
+cudaError_t launch_quantize_nvfp4_rows(const void* x, int64_t R, int64_t Kd, const float* global,
+                                       void* packed, void* scales, cudaStream_t st);
+
+// Grouped MLP (bf16 / FP8 / NVFP4), defined in the GEMM translation units.
+size_t grouped_mlp_workspace_bytes(const moe_shape& s, const moe_layout& l, int32_t w_dtype);
+cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                               int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
+                               const void* w13, const void* w13_scales, const void* w2,
+                               const void* w2_scales, const moe_nvfp4_globals* globals,
+                               void* workspace, void* out_fc2, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace moe

@@ -1,0 +1,529 @@
+// permute.cu -- dispatch_with_permute, combine with unpermute, and the FP8 /
+// NVFP4 quantizers.  All HBM-bound: 128-bit vector loads and stores, one warp
+// per token, grids sized to fill every SM.
+//
+// Follows Megatron-LM PR #6800 "Reuse caller-owned HybridEP dispatch and expert
+// output buffers" (Summary: dispatch writes permuted tokens into a caller
+// buffer; combine performs the final read), DeepEP PR #716 "perf: reuse HybridEP
+// routing allgather buffer" (Testing: dispatch with permutation and combine with
+// unpermutation, with and without probabilities, BF16 and FP8; bitwise
+// dispatched rows) and TensorRT-LLM PR #16190 "Update CuTeDSL MegaMoE kernels"
+// (TopkReduce combine; NVFP4 block scales with a global scale).
+#include <algorithm>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxK = 128;
+constexpr int kUnroll = 4;  // 16-byte vectors in flight per lane per chunk
+
+struct DispatchParams {
+  int format;
+  const float* probs;
+  int64_t T, H, E, K, cap;
+  const int32_t* row_of;
+  const int32_t* offsets;
+  const int32_t* counts;
+  const uint8_t* x;
+  const float* x_scales;  // FP8 passthrough scales, or the NVFP4 global scale
+  uint8_t* out;
+  float* out_probs;
+  uint8_t* out_scales;
+  int64_t row_bytes;    // bytes of one output row
+  int64_t scale_bytes;  // bytes of one output scale row
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_vec(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Destination rows of token t into this warp's shared slots; also writes the
+// dispatched probabilities.  Returns nothing; callers __syncwarp afterwards.
+__device__ __forceinline__ void load_dests(const DispatchParams& p, const int32_t* soff, int64_t t,
+                                           int32_t* sdest) {
+  const int lane = threadIdx.x & 31;
+  for (int k = lane; k < p.K; k += 32) {
+    const int32_t d = p.row_of[t * p.K + k];
+    sdest[k] = d;
+    if (d >= 0 && p.out_probs && p.probs) {
+      float pr;
+      if (p.format == MOE_ROUTING_DENSE_I16)
+        pr = p.probs[t * p.K + k];
+      else
+        pr = p.probs[t * p.E + expert_of_row(soff, (int)p.E, d)];
+      p.out_probs[d] = pr;
+    }
+  }
+  __syncwarp();
+}
+
+// Zero the pad rows of expert e (tokens, scales, probabilities).
+__device__ __forceinline__ void zero_pads(const DispatchParams& p, const int32_t* soff, int e) {
+  const int lane = threadIdx.x & 31;
+  const int64_t beg = (int64_t)soff[e] + p.counts[e];
+  const int64_t end = min64(soff[e + 1], p.cap);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t r = beg; r < end; r++) {
+    uint8_t* row = p.out + r * p.row_bytes;
+    for (int64_t v = lane; v < p.row_bytes / 16; v += 32) st_vec(row + v * 16, z);
+    if (p.out_scales) {
+      uint8_t* srow = p.out_scales + r * p.scale_bytes;
+      for (int64_t b = lane; b < p.scale_bytes; b += 32) srow[b] = 0;
+    }
+    if (p.out_probs && lane == 0) p.out_probs[r] = 0.0f;
+  }
+}
+
+// BF16 or FP8 rows copied bit for bit (plus FP8 scale rows).
+__global__ void __launch_bounds__(kThreads) dispatch_copy_kernel(DispatchParams p) {
+  __shared__ int32_t s_dest[kWarps][kMaxK];
+  extern __shared__ int32_t soff[];
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) soff[i] = p.offsets[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nvec = p.row_bytes / 16;
+  const int64_t nsc = p.scale_bytes / 4;
+  const int64_t items = p.T + p.E;
+  for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
+    if (it >= p.T) {
+      zero_pads(p, soff, (int)(it - p.T));
+      continue;
+    }
+    const int64_t t = it;
+    load_dests(p, soff, t, s_dest[warp]);
+    const uint8_t* src = p.x + t * p.row_bytes;
+    for (int64_t base = 0; base < nvec; base += 32 * kUnroll) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; u++) {
+        const int64_t idx = base + u * 32 + lane;
+        if (idx < nvec) v[u] = ld_stream(src + idx * 16);
+      }
+      for (int k = 0; k < p.K; k++) {
+        const int32_t d = s_dest[warp][k];
+        if (d < 0) continue;
+        uint8_t* dst = p.out + (int64_t)d * p.row_bytes;
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+          const int64_t idx = base + u * 32 + lane;
+          if (idx < nvec) st_vec(dst + idx * 16, v[u]);
+        }
+      }
+    }
+    if (nsc) {
+      const float* ssrc = p.x_scales + t * nsc;
+      for (int64_t b = lane; b < nsc; b += 32) {
+        const float sv = ssrc[b];
+        for (int k = 0; k < p.K; k++) {
+          const int32_t d = s_dest[warp][k];
+          if (d >= 0) reinterpret_cast<float*>(p.out_scales + (int64_t)d * p.scale_bytes)[b] = sv;
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// bf16 rows quantized to E4M3 with one fp32 scale per 128 elements, then
+// scattered.  A lane holds 8 elements; 16 lanes hold one 128-element block.
+__global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchParams p) {
+  __shared__ int32_t s_dest[kWarps][kMaxK];
+  extern __shared__ int32_t soff[];
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) soff[i] = p.offsets[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t H = p.H;
+  const int64_t items = p.T + p.E;
+  for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
+    if (it >= p.T) {
+      zero_pads(p, soff, (int)(it - p.T));
+      continue;
+    }
+    const int64_t t = it;
+    load_dests(p, soff, t, s_dest[warp]);
+    const uint8_t* src = p.x + t * H * 2;
+    for (int64_t base = 0; base < H; base += 256 * 2) {
+      uint2 q[2];
+      float sc[2];
+      bool live[2];
+#pragma unroll
+      for (int u = 0; u < 2; u++) {
+        const int64_t e0 = base + u * 256 + lane * 8;
+        live[u] = e0 < H;  // H is a multiple of 128, so a 16-lane block is live or dead as a whole
+        uint4 v = live[u] ? ld_stream(src + e0 * 2) : make_uint4(0, 0, 0, 0);
+        float f[8];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          f[2 * j] = bf16_bits_to_float(w[j] & 0xffffu);
+          f[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+        for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+        sc[u] = s;
+        uint32_t c[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) c[j] = e4m3x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
+        q[u] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+      }
+      for (int k = 0; k < p.K; k++) {
+        const int32_t d = s_dest[warp][k];
+        if (d < 0) continue;
+        uint8_t* dst = p.out + (int64_t)d * H;
+        float* sdst = reinterpret_cast<float*>(p.out_scales + (int64_t)d * p.scale_bytes);
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+          if (!live[u]) continue;
+          const int64_t e0 = base + u * 256 + lane * 8;
+          *reinterpret_cast<uint2*>(dst + e0) = q[u];
+          if ((lane & 15) == 0) sdst[e0 / 128] = sc[u];
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// bf16 rows quantized to NVFP4 (E2M1 + one E4M3 scale per 16 elements + the
+// fp32 global scale), then scattered.  A lane holds 8 elements; 2 lanes hold
+// one 16-element block.
+__global__ void __launch_bounds__(kThreads) dispatch_nvfp4_kernel(DispatchParams p) {
+  __shared__ int32_t s_dest[kWarps][kMaxK];
+  extern __shared__ int32_t soff[];
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) soff[i] = p.offsets[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t H = p.H;
+  const float g = *p.x_scales;
+  const int64_t items = p.T + p.E;
+  for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
+    if (it >= p.T) {
+      zero_pads(p, soff, (int)(it - p.T));
+      continue;
+    }
+    const int64_t t = it;
+    load_dests(p, soff, t, s_dest[warp]);
+    const uint8_t* src = p.x + t * H * 2;
+    for (int64_t base = 0; base < H; base += 256) {
+      const int64_t e0 = base + lane * 8;
+      const bool live = e0 < H;
+      uint4 v = live ? ld_stream(src + e0 * 2) : make_uint4(0, 0, 0, 0);
+      float f[8];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        f[2 * j] = bf16_bits_to_float(w[j] & 0xffffu);
+        f[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(f[j]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      const uint32_t scode = e4m3x2(__fdiv_rn(amax, 6.0f * g), 0.0f) & 0xffu;
+      const float denom = e4m3_to_float(scode) * g;
+      uint32_t packed = 0;
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const uint32_t b = (denom == 0.0f)
+                               ? 0u
+                               : e2m1x2(__fdiv_rn(f[2 * j], denom), __fdiv_rn(f[2 * j + 1], denom));
+        packed |= b << (8 * j);
+      }
+      for (int k = 0; k < p.K; k++) {
+        const int32_t d = s_dest[warp][k];
+        if (d < 0 || !live) continue;
+        *reinterpret_cast<uint32_t*>(p.out + (int64_t)d * (H / 2) + e0 / 2) = packed;
+        if ((lane & 1) == 0) p.out_scales[(int64_t)d * (H / 16) + e0 / 16] = (uint8_t)scode;
+      }
+    }
+    __syncwarp();
+  }
+}
+
+struct CombineParams {
+  int64_t T, H, K;
+  const int32_t* row_of;
+  const uint8_t* o;
+  const float* perm_probs;
+  uint8_t* y;
+};
+
+// y[t] = bf16(sum_k w_k * O[row_k]) with fp32 accumulation in ascending k.
+__global__ void __launch_bounds__(kThreads) combine_kernel(CombineParams p) {
+  __shared__ int32_t s_row[kWarps][kMaxK];
+  __shared__ float s_w[kWarps][kMaxK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nvec = p.H / 8;
+  for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < p.T; t += (int64_t)gridDim.x * kWarps) {
+    int nk = 0;
+    for (int k0 = 0; k0 < p.K; k0 += 32) {
+      const int k = k0 + lane;
+      int32_t r = (k < p.K) ? p.row_of[t * p.K + k] : -1;
+      const unsigned keep = __ballot_sync(0xffffffffu, r >= 0);
+      if (r >= 0) {
+        const int slot = nk + __popc(keep & lanemask_lt());  // kept routes, ascending k
+        s_row[warp][slot] = r;
+        s_w[warp][slot] = p.perm_probs ? p.perm_probs[r] : 1.0f;
+      }
+      nk += __popc(keep);
+    }
+    __syncwarp();
+    for (int64_t base = 0; base < nvec; base += 64) {
+      float acc[2][8];
+#pragma unroll
+      for (int u = 0; u < 2; u++)
+#pragma unroll
+        for (int j = 0; j < 8; j++) acc[u][j] = 0.0f;
+      for (int k0 = 0; k0 < nk; k0 += 8) {
+        uint4 v[8][2];
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {
+          if (k0 + kk < nk) {
+            const uint8_t* row = p.o + (int64_t)s_row[warp][k0 + kk] * p.H * 2;
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+              const int64_t idx = base + u * 32 + lane;
+              if (idx < nvec) v[kk][u] = ld_stream(row + idx * 16);
+            }
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {
+          if (k0 + kk < nk) {
+            const float wk = s_w[warp][k0 + kk];
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+              const uint32_t w4[4] = {v[kk][u].x, v[kk][u].y, v[kk][u].z, v[kk][u].w};
+#pragma unroll
+              for (int j = 0; j < 4; j++) {
+                acc[u][2 * j] = fmaf(wk, bf16_bits_to_float(w4[j] & 0xffffu), acc[u][2 * j]);
+                acc[u][2 * j + 1] = fmaf(wk, bf16_bits_to_float(w4[j] >> 16), acc[u][2 * j + 1]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; u++) {
+        const int64_t idx = base + u * 32 + lane;
+        if (idx < nvec) {
+          uint4 out;
+          out.x = float_to_bf16_bits(acc[u][0]) | (float_to_bf16_bits(acc[u][1]) << 16);
+          out.y = float_to_bf16_bits(acc[u][2]) | (float_to_bf16_bits(acc[u][3]) << 16);
+          out.z = float_to_bf16_bits(acc[u][4]) | (float_to_bf16_bits(acc[u][5]) << 16);
+          out.w = float_to_bf16_bits(acc[u][6]) | (float_to_bf16_bits(acc[u][7]) << 16);
+          st_vec(p.y + t * p.H * 2 + idx * 16, out);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// One CTA per 128x128 block of a bf16 weight [G][N][Kd]: fp32 scale amax/448
+// (1 for an all-zero block) and E4M3 codes of w / scale.
+__global__ void __launch_bounds__(256) quantize_fp8_blocks_kernel(const uint8_t* w, int64_t N,
+                                                                  int64_t Kd, uint8_t* codes,
+                                                                  float* scales) {
+  __shared__ float s_max[8];
+  const int64_t kb = blockIdx.x, nb = blockIdx.y, g = blockIdx.z;
+  const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int64_t r = g * N + nb * 128 + row;
+  const uint8_t* src = w + (r * Kd + kb * 128 + half * 64) * 2;
+  float f[64];
+  float amax = 0.0f;
+#pragma unroll
+  for (int v = 0; v < 8; v++) {
+    const uint4 q = ld_stream(src + v * 16);
+    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      f[v * 8 + 2 * j] = bf16_bits_to_float(w4[j] & 0xffffu);
+      f[v * 8 + 2 * j + 1] = bf16_bits_to_float(w4[j] >> 16);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 64; j++) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = s_max[0];
+#pragma unroll
+  for (int i = 1; i < 8; i++) amax = fmaxf(amax, s_max[i]);
+  const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+  uint8_t* dst = codes + r * Kd + kb * 128 + half * 64;
+#pragma unroll
+  for (int v = 0; v < 4; v++) {
+    uint4 o;
+    uint32_t c[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) c[j] = e4m3x2(__fdiv_rn(f[v * 16 + 2 * j], s), __fdiv_rn(f[v * 16 + 2 * j + 1], s));
+    o.x = c[0] | (c[1] << 16);
+    o.y = c[2] | (c[3] << 16);
+    o.z = c[4] | (c[5] << 16);
+    o.w = c[6] | (c[7] << 16);
+    st_vec(dst + v * 16, o);
+  }
+  if (threadIdx.x == 0) scales[(g * (N / 128) + nb) * (Kd / 128) + kb] = s;
+}
+
+// One thread per 16-element block of bf16 rows [R][Kd] -> NVFP4.
+__global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const uint8_t* x, int64_t R, int64_t Kd,
+                                                                  const float* global, uint8_t* packed,
+                                                                  uint8_t* scales) {
+  const float g = *global;
+  const int64_t nblk = R * (Kd / 16);
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const uint8_t* src = x + b * 32;
+    float f[16];
+#pragma unroll
+    for (int v = 0; v < 2; v++) {
+      const uint4 q = ld_stream(src + v * 16);
+      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        f[v * 8 + 2 * j] = bf16_bits_to_float(w4[j] & 0xffffu);
+        f[v * 8 + 2 * j + 1] = bf16_bits_to_float(w4[j] >> 16);
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
+    const uint32_t scode = e4m3x2(__fdiv_rn(amax, 6.0f * g), 0.0f) & 0xffu;
+    const float denom = e4m3_to_float(scode) * g;
+    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const uint32_t c =
+          (denom == 0.0f) ? 0u : e2m1x2(__fdiv_rn(f[2 * j], denom), __fdiv_rn(f[2 * j + 1], denom));
+      if (j < 4)
+        w0 |= c << (8 * j);
+      else
+        w1 |= c << (8 * (j - 4));
+    }
+    *reinterpret_cast<uint2*>(packed + b * 8) = make_uint2(w0, w1);
+    scales[b] = (uint8_t)scode;
+  }
+}
+
+unsigned grid_for(int64_t items_warps) {
+  const int64_t per_sm = 2048 / kThreads;
+  int64_t blocks = (items_warps + kWarps - 1) / kWarps;
+  const int64_t cap = (int64_t)device_sm_count() * per_sm;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (unsigned)blocks;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                            int32_t in_dtype, const void* x, const void* x_scales,
+                            const moe_routing& r, void* out_tokens, float* out_probs,
+                            void* out_scales, cudaStream_t st) {
+  DispatchParams p;
+  p.format = r.format;
+  p.probs = r.probs;
+  p.T = s.T;
+  p.H = s.H;
+  p.E = s.E;
+  p.K = s.K;
+  p.cap = l.capacity;
+  p.row_of = h.row_of;
+  p.offsets = h.padded_offsets;
+  p.counts = h.tokens_per_expert;
+  p.x = static_cast<const uint8_t*>(x);
+  p.x_scales = static_cast<const float*>(x_scales);
+  p.out = static_cast<uint8_t*>(out_tokens);
+  p.out_probs = out_probs;
+  p.out_scales = static_cast<uint8_t*>(out_scales);
+  const unsigned grid = grid_for(s.T + s.E);
+  const size_t smem = (size_t)(s.E + 1) * 4;
+  switch (in_dtype) {
+    case MOE_DTYPE_BF16:
+      p.row_bytes = s.H * 2;
+      p.scale_bytes = 0;
+      p.out_scales = nullptr;
+      dispatch_copy_kernel<<<grid, kThreads, smem, st>>>(p);
+      break;
+    case MOE_DTYPE_FP8_E4M3_B128:
+      p.row_bytes = s.H;
+      p.scale_bytes = (s.H / 128) * 4;
+      dispatch_copy_kernel<<<grid, kThreads, smem, st>>>(p);
+      break;
+    case MOE_DTYPE_BF16_TO_FP8:
+      p.row_bytes = s.H;
+      p.scale_bytes = (s.H / 128) * 4;
+      dispatch_fp8_kernel<<<grid, kThreads, smem, st>>>(p);
+      break;
+    case MOE_DTYPE_BF16_TO_NVFP4:
+      p.row_bytes = s.H / 2;
+      p.scale_bytes = s.H / 16;
+      dispatch_nvfp4_kernel<<<grid, kThreads, smem, st>>>(p);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                           const void* expert_out, const float* perm_probs, void* y,
+                           cudaStream_t st) {
+  (void)l;
+  CombineParams p;
+  p.T = s.T;
+  p.H = s.H;
+  p.K = s.K;
+  p.row_of = h.row_of;
+  p.o = static_cast<const uint8_t*>(expert_out);
+  p.perm_probs = perm_probs;
+  p.y = static_cast<uint8_t*>(y);
+  combine_kernel<<<grid_for(s.T), kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8_blocks(const void* w, int64_t G, int64_t N, int64_t Kd, void* codes,
+                                       float* scales, cudaStream_t st) {
+  if (G == 0 || N == 0 || Kd == 0) return cudaSuccess;
+  dim3 grid((unsigned)(Kd / 128), (unsigned)(N / 128), (unsigned)G);
+  quantize_fp8_blocks_kernel<<<grid, 256, 0, st>>>(static_cast<const uint8_t*>(w), N, Kd,
+                                                   static_cast<uint8_t*>(codes), scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_nvfp4_rows(const void* x, int64_t R, int64_t Kd, const float* global,
+                                       void* packed, void* scales, cudaStream_t st) {
+  const int64_t nblk = R * (Kd / 16);
+  int64_t blocks = (nblk + 255) / 256;
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  quantize_nvfp4_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+      static_cast<const uint8_t*>(x), R, Kd, global, static_cast<uint8_t*>(packed),
+      static_cast<uint8_t*>(scales));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,62 @@
+"""Helpers shared by the GPU parity tests: run the library on seeded inputs and
+read its device outputs back as numpy arrays for comparison with the oracle."""
+import numpy as np
+import torch
+
+import workloads
+
+
+def moe_mod():
+    from permute_grouped_expert_gb300 import _build
+
+    _build.build()
+    import permute_grouped_expert_gb300 as moe
+
+    return moe
+
+
+def fill_pattern(t: torch.Tensor) -> torch.Tensor:
+    """Pre-fill an output with 0xFF bytes so untouched rows are recognisable."""
+    t.view(torch.uint8).fill_(0xFF)
+    return t
+
+
+def preprocess(moe, w, fmt, rmap, probs, cap, dev="cuda"):
+    shape = moe.Shape(w.T, w.H, w.E, w.K, w.I)
+    layout = moe.Layout(w.m, cap)
+    routing = moe.Routing(fmt, torch.from_numpy(np.ascontiguousarray(rmap)).to(dev),
+                          None if probs is None else torch.from_numpy(probs).to(dev))
+    handle = moe.Handle.empty(shape, layout, dev)
+    for f in ("row_of", "token_of", "slot_of"):
+        getattr(handle, f).fill_(-7)
+    ws = torch.empty(moe.moe_preprocess_workspace_size(shape), dtype=torch.uint8, device=dev)
+    moe.moe_preprocess(routing, shape, layout, handle, ws)
+    return shape, layout, routing, handle, ws
+
+
+def handle_np(handle, T, K, cap):
+    torch.cuda.synchronize()
+    total = int(handle.total_rows.item())
+    valid = min(total, cap)
+    return dict(counts=handle.tokens_per_expert.cpu().numpy(), offsets=handle.padded_offsets.cpu().numpy(),
+                row_of=handle.row_of.cpu().numpy()[:T * K].reshape(T, K),
+                token_of=handle.token_of.cpu().numpy()[:valid], slot_of=handle.slot_of.cpu().numpy()[:valid],
+                total_rows=total, overflow=int(handle.overflow.item()), status=int(handle.status.item()),
+                valid_rows=valid)
+
+
+def assert_handle_equal(got, ref):
+    for key in ("counts", "offsets", "row_of", "token_of", "slot_of"):
+        assert np.array_equal(got[key], ref[key]), key
+    for key in ("total_rows", "overflow", "status"):
+        assert got[key] == ref[key], (key, got[key], ref[key])
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return workloads.bf16_bits(t.cpu())
+
+
+def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    """max |got - ref| / rms(ref): the tolerance measure for floating outputs."""
+    rms = np.sqrt(np.mean(np.square(ref))) if ref.size else 0.0
+    return float(np.abs(got - ref).max() / rms) if ref.size and rms > 0 else float(np.abs(got - ref).max(initial=0))

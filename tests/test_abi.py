@@ -1,0 +1,168 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every function include/moe.h declares; argument validation rejects bad
+calls before anything is enqueued; host helpers (capacity rule, routing-map
+bytes, buffer ring) behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from permute_grouped_expert_gb300 import _build
+
+    _build.build()
+    import permute_grouped_expert_gb300 as m
+
+    return m
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(moe_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(moe):
+    names = declared_functions()
+    assert len(names) >= 16, names
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.exported_symbols())
+
+
+def test_capacity_rule_golden(moe):
+    path = os.path.join(ROOT, "tests", "golden", "capacity.txt")
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        rows, factor, align, cap = line.split()
+        assert moe.moe_capacity(int(rows), float(factor), int(align)) == int(cap)
+    with pytest.raises(moe.MoeError):
+        moe.moe_capacity(-1, 1.5, 4)
+    with pytest.raises(moe.MoeError):
+        moe.moe_capacity(10, 0.0, 4)
+
+
+def test_routing_map_bytes_golden(moe):
+    path = os.path.join(ROOT, "tests", "golden", "routing_bytes.txt")
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        layout, T, E, K, nbytes = line.split()
+        fmt = moe.ROUTING_SPARSE_BOOL if layout == "sparse" else moe.ROUTING_DENSE_I16
+        assert moe.moe_routing_map_bytes(fmt, int(T), int(E), int(K)) == int(nbytes)
+
+
+def test_workspace_queries(moe):
+    s = moe.Shape(T=8192, H=7168, E=32, K=8, I=2048)
+    assert moe.moe_preprocess_workspace_size(s) > 8192 * 8 * 2
+    lay = moe.Layout(32, 70000)
+    assert moe.moe_grouped_mlp_workspace_size(s, lay, moe.DTYPE_BF16) >= 70000 * 2048 * 2
+    with pytest.raises(moe.MoeError):
+        moe.moe_preprocess_workspace_size(moe.Shape(T=8, H=128, E=2000, K=2))
+    with pytest.raises(moe.MoeError):
+        moe.moe_grouped_mlp_workspace_size(moe.Shape(T=8, H=128, E=4, K=2, I=100), lay, moe.DTYPE_BF16)
+
+
+def _c_call(moe, fn, *args):
+    return getattr(moe.library(), fn)(*args)
+
+
+def test_validation_rejects_before_any_launch(moe):
+    """Bad arguments return MOE_ERR_INVALID_ARG without touching the GPU
+    (these pointers are never dereferenced)."""
+    fake = ctypes.c_void_p(0x1000)
+    good_shape = moe._Shape(64, 256, 8, 2, 128)
+    good_layout = moe._Layout(32, 1024)
+    routing = moe._Routing(0, fake, None)
+    handle = moe._HandleDev(*([fake] * 8))
+    byref = ctypes.byref
+    lib = moe.library()
+    # null routing map
+    assert lib.moe_preprocess(byref(moe._Routing(0, None, None)), byref(good_shape), byref(good_layout),
+                              byref(handle), fake, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    # bad routing format
+    assert lib.moe_preprocess(byref(moe._Routing(7, fake, None)), byref(good_shape), byref(good_layout),
+                              byref(handle), fake, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    # K > E
+    assert lib.moe_preprocess(byref(routing), byref(moe._Shape(64, 256, 2, 4, 0)), byref(good_layout),
+                              byref(handle), fake, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    # negative capacity / zero pad multiple
+    assert lib.moe_preprocess(byref(routing), byref(good_shape), byref(moe._Layout(32, -1)), byref(handle), fake,
+                              1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_preprocess(byref(routing), byref(good_shape), byref(moe._Layout(0, 10)), byref(handle), fake,
+                              1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    # workspace too small
+    assert lib.moe_preprocess(byref(routing), byref(good_shape), byref(good_layout), byref(handle), fake, 16,
+                              None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    # missing handle array
+    h2 = moe._HandleDev(*([fake] * 7 + [None]))
+    assert lib.moe_preprocess(byref(routing), byref(good_shape), byref(good_layout), byref(h2), fake, 1 << 30,
+                              None) == moe.MOE_ERR_INVALID_ARG
+    # H not a multiple of 128; misaligned rows; unknown dtype
+    assert lib.moe_dispatch_permute(byref(handle), byref(moe._Shape(64, 100, 8, 2, 0)), byref(good_layout),
+                                    moe.DTYPE_BF16, fake, None, byref(routing), fake, None, None,
+                                    None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_permute(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16,
+                                    ctypes.c_void_p(0x1008), None, byref(routing), fake, None, None,
+                                    None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_permute(byref(handle), byref(good_shape), byref(good_layout), 99, fake, None,
+                                    byref(routing), fake, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    # FP8 dispatch without output scales
+    assert lib.moe_dispatch_permute(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16_TO_FP8,
+                                    fake, None, byref(routing), fake, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    # grouped MLP: I not a multiple of 128, workspace misaligned, NVFP4 without globals
+    assert lib.moe_grouped_mlp(byref(handle), byref(moe._Shape(64, 256, 8, 2, 100)), byref(good_layout),
+                               moe.DTYPE_BF16, fake, None, fake, None, fake, None, None, fake, 1 << 30, fake,
+                               None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_mlp(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16, fake, None,
+                               fake, None, fake, None, None, ctypes.c_void_p(0x1010), 1 << 30, fake,
+                               None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_mlp(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_NVFP4, fake, fake,
+                               fake, fake, fake, fake, None, fake, 1 << 30, fake, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_mlp(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16, fake, None,
+                               fake, None, fake, None, None, fake, 8, fake,
+                               None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    # combine with a null expert buffer
+    assert lib.moe_combine_unpermute(byref(handle), byref(good_shape), byref(good_layout), None, None, fake,
+                                     None) == moe.MOE_ERR_INVALID_ARG
+    # quantizers: shapes not multiples of the block
+    assert lib.moe_quantize_fp8_blocks(fake, 1, 100, 128, fake, fake, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_nvfp4_rows(fake, 4, 24, fake, fake, fake, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_ring_rotation_and_lifetime_errors(moe):
+    """Round-robin slots; acquiring a held slot is early reuse; releasing a
+    free slot is a double release; neither changes the ring."""
+    r = moe.Ring(3, use_events=False)
+    assert [r.acquire(), r.acquire(), r.acquire()] == [0, 1, 2]
+    with pytest.raises(moe.MoeError) as ei:
+        r.acquire()
+    assert ei.value.status == moe.MOE_ERR_RING_EARLY_REUSE
+    r.release(0)
+    with pytest.raises(moe.MoeError) as ei:
+        r.release(0)
+    assert ei.value.status == moe.MOE_ERR_RING_DOUBLE_RELEASE
+    assert r.acquire() == 0          # slot 0 is free again, next in order
+    with pytest.raises(moe.MoeError) as ei:
+        r.acquire()                  # slot 1 is still held by its first producer
+    assert ei.value.status == moe.MOE_ERR_RING_EARLY_REUSE
+    r.release(1)
+    r.release(2)
+    assert r.acquire() == 1
+    with pytest.raises(moe.MoeError):
+        r.release(7)
+    r.close()
+    with pytest.raises(moe.MoeError):
+        moe.Ring(0, use_events=False)
