@@ -7,9 +7,9 @@ import workloads
 
 
 def moe_mod():
-    from permute_grouped_expert_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__.build_library()
     import permute_grouped_expert_gb300 as moe
 
     return moe

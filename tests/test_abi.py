@@ -13,9 +13,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def moe():
-    from permute_grouped_expert_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__.build_library()
     import permute_grouped_expert_gb300 as m
 
     return m
