@@ -1,17 +1,45 @@
-// grouped_mlp.cu -- placeholder until the tcgen05 grouped GEMMs land.
+// grouped_mlp.cu -- workspace sizing and per-format dispatch of the grouped
+// SwiGLU expert MLP (FC1 -> SwiGLU -> FC2).
 #include "moe_internal.h"
 
 namespace moe {
 
+cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                                    const void* perm_tokens, const void* w13, const void* w2, void* act,
+                                    void* out_fc2, cudaStream_t st);
+
+namespace {
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+}  // namespace
+
 size_t grouped_mlp_workspace_bytes(const moe_shape& s, const moe_layout& l, int32_t w_dtype) {
-  (void)w_dtype;
-  return (size_t)l.capacity * (size_t)s.I * 2 + 1024;
+  const size_t cap = (size_t)l.capacity, I = (size_t)s.I;
+  switch (w_dtype) {
+    case MOE_DTYPE_BF16:
+      return round_up(cap * I * 2, 1024) + 1024;
+    case MOE_DTYPE_FP8_E4M3_B128:  // E4M3 intermediate + fp32 scales per 128 elements
+      return round_up(cap * I, 1024) + round_up(cap * (I / 128) * 4, 1024) + 1024;
+    case MOE_DTYPE_NVFP4:  // packed E2M1 intermediate + E4M3 scales per 16 elements
+      return round_up(cap * I / 2, 1024) + round_up(cap * (I / 16), 1024) + 1024;
+  }
+  return 0;
 }
 
-cudaError_t launch_grouped_mlp(const moe_handle_dev&, const moe_shape&, const moe_layout&, int32_t,
-                               const void*, const void*, const void*, const void*, const void*,
-                               const void*, const moe_nvfp4_globals*, void*, void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                               int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
+                               const void* w13, const void* w13_scales, const void* w2,
+                               const void* w2_scales, const moe_nvfp4_globals* globals,
+                               void* workspace, void* out_fc2, cudaStream_t st) {
+  (void)perm_scales;
+  (void)w13_scales;
+  (void)w2_scales;
+  (void)globals;
+  switch (w_dtype) {
+    case MOE_DTYPE_BF16:
+      return launch_grouped_mlp_bf16(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
+    default:
+      return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace moe

@@ -116,7 +116,7 @@ MOE_DEVICE uint64_t smem_desc_sw128(uint32_t saddr) {
 // Instruction descriptor of a dense kind::f16 MMA: bf16 x bf16 -> fp32, both
 // operands K-major.  [4,6) D format (1 = f32), [7,10) A format (1 = bf16),
 // [10,13) B format, [17,23) N>>3, [24,29) M>>4.
-constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 

@@ -1,0 +1,141 @@
+"""GPU parity of the grouped SwiGLU expert MLP (tcgen05 grouped GEMMs) and of
+the whole layer against the CPU oracle: max-abs-error / RMS of the output
+<= 1e-2 for bf16 (<= 5e-2 for FP8 / NVFP4), fp32 accumulation on the GPU."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import bits, fill_pattern, handle_np, moe_mod, preprocess, rel_err
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 1e-2
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return moe_mod()
+
+
+def _case(name, **kw):
+    return workloads.scaled(workloads.WORKLOADS[name], **kw)
+
+
+def run_layer_bf16(moe, w, seed, cap=None, routing=None):
+    """The four calls on seeded inputs; returns everything the checks need."""
+    fmt, rmap, probs = workloads.routing_inputs(w, seed, routing)
+    cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m) if cap is None else cap
+    x = workloads.activations(w, seed)
+    w13, w2 = workloads.expert_weights(w, seed, device="cuda")
+    shape, layout, routing_t, handle, _ = preprocess(moe, w, fmt, rmap, probs, cap)
+    y = fill_pattern(torch.empty(max(cap, 1), w.H, dtype=torch.bfloat16, device="cuda"))
+    yp = torch.empty(max(cap, 1), dtype=torch.float32, device="cuda")
+    moe.moe_dispatch_permute(handle, shape, layout, moe.DTYPE_BF16, x.cuda(), None, routing_t, y, yp)
+    ws = fill_pattern(torch.empty(moe.moe_grouped_mlp_workspace_size(shape, layout, moe.DTYPE_BF16),
+                                  dtype=torch.uint8, device="cuda"))
+    o = fill_pattern(torch.empty(max(cap, 1), w.H, dtype=torch.bfloat16, device="cuda"))
+    moe.moe_grouped_mlp(handle, shape, layout, moe.DTYPE_BF16, y, None, w13, None, w2, None, None, ws, o)
+    out = fill_pattern(torch.empty(max(w.T, 1), w.H, dtype=torch.bfloat16, device="cuda"))
+    moe.moe_combine_unpermute(handle, shape, layout, o, yp, out)
+    torch.cuda.synchronize()
+    return dict(fmt=fmt, rmap=rmap, probs=probs, cap=cap, x=x, w13=w13, w2=w2, handle=handle, o=o, out=out[:w.T])
+
+
+@pytest.mark.parametrize("name,w", [
+    ("tiny", _case("tiny")),
+    ("ragged_h384", _case("tiny", T=200, H=384, E=5, K=2, I=128)),
+    ("one_expert", _case("tiny", T=300, H=256, E=1, K=1, I=256)),
+    ("m1_no_padding", _case("tiny", T=257, H=256, E=7, K=3, I=128, m=1)),
+], ids=lambda v: v if isinstance(v, str) else "")
+def test_grouped_mlp_bf16_all_rows(oracle, moe, name, w):
+    r = run_layer_bf16(moe, w, seed=21)
+    pre = oracle.preprocess(r["fmt"], r["rmap"], w.T, w.E, w.K, w.m, r["cap"])
+    yo, po = oracle.dispatch(r["fmt"], r["rmap"], r["probs"], pre, workloads.bf16_bits(r["x"]), r["cap"], w.E, w.K)
+    v = pre["valid_rows"]
+    w13b, w2b = workloads.bf16_bits(r["w13"]), workloads.bf16_bits(r["w2"])
+    ob, _ = oracle.grouped_mlp_rows(0, yo, None, w.H, w.I, w.E, pre["offsets"], w13b, None, w2b, None,
+                                    np.arange(v))
+    got = bits(r["o"])
+    assert rel_err(oracle.bf16_to_f64(got[:v]), oracle.bf16_to_f64(ob)) <= TOL_BF16
+    # pad rows are exactly zero; rows past the segments untouched
+    for e in range(w.E):
+        for row in range(pre["offsets"][e] + pre["counts"][e], min(pre["offsets"][e + 1], r["cap"])):
+            assert not got[row].any()
+    assert np.all(got[v:] == 0xFFFF)
+    # whole layer vs the unpermuted per-token formulation of the oracle
+    ref = oracle.layer_per_token(0, r["fmt"], r["rmap"], r["probs"], w.E, w.K, workloads.bf16_bits(r["x"]), None,
+                                 w.H, w.I, w13b, None, w2b, None, np.arange(w.T))
+    assert rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(ref)) <= TOL_BF16
+
+
+def _sampled_check(oracle, w, r, n_tokens=48, seed=0):
+    """Oracle on a sample of tokens (all their routes) at full size."""
+    pre = oracle.preprocess(r["fmt"], r["rmap"], w.T, w.E, w.K, w.m, r["cap"])
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(w.T, n_tokens, replace=False))
+    rows = np.unique(pre["row_of"][toks][pre["row_of"][toks] >= 0])
+    xb = workloads.bf16_bits(r["x"])
+    yo, po = oracle.dispatch(r["fmt"], r["rmap"], r["probs"], pre, xb, r["cap"], w.E, w.K)
+    experts = sorted({int(np.searchsorted(pre["offsets"], rr, side="right") - 1) for rr in rows})
+    # oracle weights for the experts involved only, remapped to local ids
+    w13l = workloads.bf16_bits(r["w13"][experts])
+    w2l = workloads.bf16_bits(r["w2"][experts])
+    local_off = np.zeros(len(experts) + 1, np.int32)
+    # give each involved expert its own contiguous block of the sampled rows
+    sel_rows, blocks = [], []
+    for j, e in enumerate(experts):
+        rr = rows[(rows >= pre["offsets"][e]) & (rows < pre["offsets"][e + 1])]
+        sel_rows.append(rr)
+        local_off[j + 1] = local_off[j] + len(rr)
+    sel = np.concatenate(sel_rows)
+    ob, _ = oracle.grouped_mlp_rows(0, yo[sel], None, w.H, w.I, len(experts), local_off, w13l, None, w2l, None,
+                                    np.arange(len(sel)))
+    got = bits(r["o"][torch.from_numpy(sel).cuda()])
+    assert rel_err(oracle.bf16_to_f64(got), oracle.bf16_to_f64(ob)) <= TOL_BF16
+    # combine of the sampled tokens from the oracle's own expert rows
+    o_full = np.zeros((r["cap"], w.H), np.uint16)
+    o_full[sel] = ob
+    yref = oracle.combine(o_full, pre["row_of"][toks], po)
+    assert rel_err(oracle.bf16_to_f64(bits(r["out"][torch.from_numpy(toks).cuda()])),
+                   oracle.bf16_to_f64(yref)) <= TOL_BF16
+
+
+def test_mid_layer_full_size_sampled(oracle, moe):
+    """4096 tokens, hidden 2048, 64 experts, top-8, sparse map, intermediate 1024,
+    capacity factor 1.5 from a calibration pass: flag 0; sampled rows match."""
+    w = workloads.WORKLOADS["mid"]
+    fmt, rmap, probs = workloads.routing_inputs(w, 31)
+    rows = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, 1 << 30)["total_rows"]
+    cap = oracle.capacity(rows, w.cap_factor)
+    r = run_layer_bf16(moe, w, seed=31, cap=cap)
+    assert handle_np(r["handle"], w.T, w.K, cap)["overflow"] == 0
+    _sampled_check(oracle, w, r)
+
+
+def test_skewed_experts_with_empty_ones(oracle, moe):
+    """Zipf-skewed popularity over 64 experts (some empty, one very large)."""
+    w = _case("dsv3", T=2048, H=512, E=64, K=4, I=256, dtype="bf16")
+    r = run_layer_bf16(moe, w, seed=41)
+    pre = oracle.preprocess(r["fmt"], r["rmap"], w.T, w.E, w.K, w.m, r["cap"])
+    assert pre["counts"].max() > 8 * np.median(pre["counts"])
+    _sampled_check(oracle, w, r, n_tokens=64)
+
+
+def test_overflowed_capacity_layer(oracle, moe):
+    """Capacity below the routed rows: dropped routes contribute nothing."""
+    w = _case("tiny", T=256, H=256, E=8, K=2, I=128)
+    fmt, rmap, probs = workloads.routing_inputs(w, 51)
+    rows = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, 1 << 30)["total_rows"]
+    cap = oracle.capacity(rows // 2, 1.0)
+    r = run_layer_bf16(moe, w, seed=51, cap=cap)
+    pre = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, cap)
+    assert pre["overflow"] == 1
+    yo, po = oracle.dispatch(fmt, rmap, probs, pre, workloads.bf16_bits(r["x"]), cap, w.E, w.K)
+    v = pre["valid_rows"]
+    ob, _ = oracle.grouped_mlp_rows(0, yo, None, w.H, w.I, w.E, pre["offsets"], workloads.bf16_bits(r["w13"]), None,
+                                    workloads.bf16_bits(r["w2"]), None, np.arange(v))
+    o_full = np.zeros((cap, w.H), np.uint16)
+    o_full[:v] = ob
+    yref = oracle.combine(o_full, pre["row_of"], po)
+    assert rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(yref)) <= TOL_BF16
