@@ -1,0 +1,492 @@
+"""Benchmark of the single-GPU MoE layer path: preprocess -> dispatch_with_permute
+-> grouped SwiGLU MLP -> combine, on seeded synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mid] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole path over one
+batch.  `value` is whole-job tokens/s with inputs resident in HBM (device-timed
+with CUDA events on the launching stream); `e2e` is the same metric through the
+same C-ABI calls with the inputs copied from pinned host memory and the result
+copied back inside the timed region.  With N > 1 (torchrun) every rank runs an
+independent replica of the workload on its own GPU (the path has no exchange
+step on one GPU), a barrier brackets the timed region, the slowest rank's time
+is used, and `value` counts every rank's tokens.
+
+`--impl reference` times the CPU oracle (a deliberately slow fp64 restatement)
+on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; permute/combine HBM GB/s; grouped-GEMM TFLOP/s vs peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129e6
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in d}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- problem
+
+class Problem:
+    """Device-resident inputs, outputs and workspaces of one MoE layer."""
+
+    def __init__(self, moe, w: workloads.Workload, seed: int, dev):
+        import torch
+
+        self.moe, self.w, self.dev = moe, w, dev
+        fmt, rmap, probs = workloads.routing_inputs(w, seed)
+        self.fmt = fmt
+        self.map_host = torch.from_numpy(np.ascontiguousarray(rmap)).pin_memory()
+        self.probs_host = torch.from_numpy(probs).pin_memory()
+        self.x_host = workloads.activations(w, seed).pin_memory()
+        self.map = self.map_host.to(dev)
+        self.probs = self.probs_host.to(dev)
+        self.x = self.x_host.to(dev)
+        self.identity = w.I == 0
+        self.shape = moe.Shape(w.T, w.H, w.E, w.K, w.I)
+        self.routing = moe.Routing(fmt, self.map, self.probs)
+        # capacity: unbounded, or ceil(rows x factor) 4-aligned from one calibration pass
+        cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
+        ws = torch.empty(moe.moe_preprocess_workspace_size(self.shape), dtype=torch.uint8, device=dev)
+        if w.cap_factor:
+            cal_layout = moe.Layout(w.m, cap)
+            h = moe.Handle.empty(self.shape, cal_layout, dev)
+            moe.moe_preprocess(self.routing, self.shape, cal_layout, h, ws)
+            torch.cuda.synchronize()
+            cap = moe.moe_capacity(int(h.total_rows.item()), w.cap_factor, 4)
+        self.cap = cap
+        self.layout = moe.Layout(w.m, cap)
+        self.ws = ws
+        self.handle = moe.Handle.empty(self.shape, self.layout, dev)
+        self.in_dtype = {"bf16": moe.DTYPE_BF16, "fp8": moe.DTYPE_BF16_TO_FP8, "nvfp4": moe.DTYPE_BF16_TO_NVFP4}[w.dtype]
+        self.w_dtype = {"bf16": moe.DTYPE_BF16, "fp8": moe.DTYPE_FP8_E4M3_B128, "nvfp4": moe.DTYPE_NVFP4}[w.dtype]
+        if w.dtype == "bf16":
+            self.y = torch.empty(cap, w.H, dtype=torch.bfloat16, device=dev)
+            self.y_scales = None
+        elif w.dtype == "fp8":
+            self.y = torch.empty(cap, w.H, dtype=torch.uint8, device=dev)
+            self.y_scales = torch.empty(cap, w.H // 128, dtype=torch.float32, device=dev)
+        else:
+            self.y = torch.empty(cap, w.H // 2, dtype=torch.uint8, device=dev)
+            self.y_scales = torch.empty(cap, w.H // 16, dtype=torch.uint8, device=dev)
+        self.yp = torch.empty(cap, dtype=torch.float32, device=dev)
+        self.out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+        self.out_host = torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory()
+        self.globals = None
+        self.x_scales = None
+        if not self.identity:
+            w13, w2 = workloads.expert_weights(w, seed, device=dev)
+            if w.dtype == "bf16":
+                self.w13, self.w2, self.w13_s, self.w2_s = w13, w2, None, None
+            elif w.dtype == "fp8":
+                self.w13 = torch.empty(w13.shape, dtype=torch.uint8, device=dev)
+                self.w13_s = torch.empty(w.E, 2 * w.I // 128, w.H // 128, dtype=torch.float32, device=dev)
+                self.w2 = torch.empty(w2.shape, dtype=torch.uint8, device=dev)
+                self.w2_s = torch.empty(w.E, w.H // 128, w.I // 128, dtype=torch.float32, device=dev)
+                moe.moe_quantize_fp8_blocks(w13, self.w13, self.w13_s)
+                moe.moe_quantize_fp8_blocks(w2, self.w2, self.w2_s)
+            else:
+                g13 = (w13.float().abs().amax(dim=(1, 2)) / (6 * 448)).contiguous()
+                g2 = (w2.float().abs().amax(dim=(1, 2)) / (6 * 448)).contiguous()
+                self.w13 = torch.empty(w.E, 2 * w.I, w.H // 2, dtype=torch.uint8, device=dev)
+                self.w13_s = torch.empty(w.E, 2 * w.I, w.H // 16, dtype=torch.uint8, device=dev)
+                self.w2 = torch.empty(w.E, w.H, w.I // 2, dtype=torch.uint8, device=dev)
+                self.w2_s = torch.empty(w.E, w.H, w.I // 16, dtype=torch.uint8, device=dev)
+                for e in range(w.E):
+                    moe.moe_quantize_nvfp4_rows(w13[e], g13[e:e + 1], self.w13[e], self.w13_s[e])
+                    moe.moe_quantize_nvfp4_rows(w2[e], g2[e:e + 1], self.w2[e], self.w2_s[e])
+                g1 = (self.x.float().abs().amax() / (6 * 448)).reshape(1)
+                self.x_scales = g1
+                self.globals = moe.Nvfp4Globals(g1, torch.tensor([0.01], device=dev), g13, g2)
+            del w13, w2
+            self.act_ws = torch.empty(moe.moe_grouped_mlp_workspace_size(self.shape, self.layout, self.w_dtype),
+                                      dtype=torch.uint8, device=dev)
+            self.o = torch.empty(cap, w.H, dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+
+    def step(self, stream, ev=None, prof=None):
+        """The four library calls; ev: list of 5 events recorded between calls."""
+        moe = self.moe
+        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        rec(0)
+        moe.moe_preprocess(self.routing, self.shape, self.layout, self.handle, self.ws, stream=stream)
+        rec(1)
+        moe.moe_dispatch_permute(self.handle, self.shape, self.layout, self.in_dtype, self.x, self.x_scales,
+                                 self.routing, self.y, self.yp, self.y_scales, stream=stream)
+        rec(2)
+        if self.identity:
+            expert_out = self.y
+        else:
+            if prof:
+                moe.moe_profile_next_grouped_mlp(*prof)
+            moe.moe_grouped_mlp(self.handle, self.shape, self.layout, self.w_dtype, self.y, self.y_scales, self.w13,
+                                self.w13_s, self.w2, self.w2_s, self.globals, self.act_ws, self.o, stream=stream)
+            expert_out = self.o
+        rec(3)
+        moe.moe_combine_unpermute(self.handle, self.shape, self.layout, expert_out, self.yp, self.out, stream=stream)
+        rec(4)
+
+    def kernels_per_step(self) -> int:
+        return 2 + 1 + (0 if self.identity else 2) + 1
+
+    def routed_rows(self) -> int:
+        import torch
+        torch.cuda.synchronize()
+        return int(self.handle.row_of[: self.w.T * self.w.K].ge(0).sum().item())
+
+    # algorithmic work per launch
+    def fc1_flops(self, R):
+        return 2.0 * R * self.w.H * 2 * self.w.I
+
+    def fc2_flops(self, R):
+        return 2.0 * R * self.w.I * self.w.H
+
+    def dispatch_bytes(self, R):
+        w = self.w
+        row_in = {"bf16": 2 * w.H, "fp8": 2 * w.H, "nvfp4": 2 * w.H}[w.dtype]
+        row_out = {"bf16": 2 * w.H, "fp8": w.H + 4 * (w.H // 128), "nvfp4": w.H // 2 + w.H // 16}[w.dtype]
+        return w.T * row_in + R * row_out + R * 4 + w.T * w.K * 4 * 2
+
+    def combine_bytes(self, R):
+        w = self.w
+        return R * 2 * w.H + R * 4 + w.T * w.K * 4 + w.T * 2 * w.H
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        __graft_entry__.build_library()
+    if world > 1:
+        dist.barrier()
+    import permute_grouped_expert_gb300 as moe
+
+    prob = Problem(moe, w, args.seed + rank, dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            prob.step(stream)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: inputs resident in HBM
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)] if not prob.identity else None
+    if pevs:
+        for trio in pevs:  # create the underlying events before handing them to the library
+            for e in trio:
+                e.record(stream)
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        t_begin.record(stream)
+        for i in range(K):
+            prob.step(stream, evs[i], pevs[i] if pevs else None)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / K
+
+    def mean_ms(a, b, table):
+        return statistics.mean(table[i][a].elapsed_time(table[i][b]) for i in range(K))
+
+    t_pre = mean_ms(0, 1, evs)
+    t_dis = mean_ms(1, 2, evs)
+    t_mlp = mean_ms(2, 3, evs)
+    t_com = mean_ms(3, 4, evs)
+    t_fc1 = mean_ms(0, 1, pevs) if pevs else None
+    t_fc2 = mean_ms(1, 2, pevs) if pevs else None
+
+    # ---- end to end: pinned host inputs in, result out, every step
+    e2e_evs = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    h2d = prob.x_host.numel() * 2 + prob.map_host.numel() * prob.map_host.element_size() + prob.probs_host.numel() * 4
+    d2h = prob.out_host.numel() * 2
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e2e_evs[0].record(stream)
+        for i in range(K):
+            prob.x.copy_(prob.x_host, non_blocking=True)
+            prob.map.copy_(prob.map_host, non_blocking=True)
+            prob.probs.copy_(prob.probs_host, non_blocking=True)
+            prob.step(stream)
+            prob.out_host.copy_(prob.out, non_blocking=True)
+        e2e_evs[1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e2e_evs[0].elapsed_time(e2e_evs[1])
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    R = prob.routed_rows()
+    overflow = int(prob.handle.overflow.item())
+    status = int(prob.handle.status.item())
+    tokens = w.T * world
+    value = tokens * K / (total_ms / 1e3)
+    peaks, peak_src = load_peaks()
+
+    breakdown = {
+        "preprocess_ms": round(t_pre, 5), "dispatch_ms": round(t_dis, 5), "combine_ms": round(t_com, 5),
+        "dispatch_gbs": round(prob.dispatch_bytes(R) / (t_dis * 1e-3) / 1e9, 1),
+        "combine_gbs": round(prob.combine_bytes(R) / (t_com * 1e-3) / 1e9, 1),
+        "routed_rows": R, "capacity": prob.cap, "overflow": overflow, "device_status": status,
+    }
+    if prob.identity:
+        dom = "dispatch_permute"
+        achieved = prob.dispatch_bytes(R) / (t_dis * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        breakdown.update({"grouped_mlp_ms": round(t_mlp, 5), "fc1_ms": round(t_fc1, 5), "fc2_ms": round(t_fc2, 5),
+                          "fc1_tflops": round(prob.fc1_flops(R) / (t_fc1 * 1e-3) / 1e12, 1),
+                          "fc2_tflops": round(prob.fc2_flops(R) / (t_fc2 * 1e-3) / 1e12, 1)})
+        achieved = prob.fc1_flops(R) / (t_fc1 * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * (2.0 if w.dtype == "fp8" else 4.0 if w.dtype == "nvfp4" else 1.0)
+        roof = {"kernel": "grouped_fc1_swiglu", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops (burst)" + (" x nominal dtype ratio" if w.dtype != "bf16" else "")}
+        breakdown["fc1_frac_of_peak"] = roof["frac"]
+        breakdown["fc2_frac_of_peak"] = round(prob.fc2_flops(R) / (t_fc2 * 1e-3) / 1e12 / peak, 4)
+    breakdown["dispatch_frac_of_hbm"] = round(breakdown["dispatch_gbs"] / peaks["hbm_gbs"], 4)
+    breakdown["combine_frac_of_hbm"] = round(breakdown["combine_gbs"] / peaks["hbm_gbs"], 4)
+
+    in_bytes = prob.x.numel() * 2 + (0 if prob.identity else sum(
+        t.numel() * t.element_size() for t in (prob.w13, prob.w2)))
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded; shapes of the pages' workloads)",
+        "config": {"workload": w.name, "tokens": w.T, "hidden": w.H, "experts": w.E, "topk": w.K,
+                   "intermediate": w.I, "pad_multiple": w.m, "routing": w.routing,
+                   "capacity_factor": w.cap_factor or None, "capacity": prob.cap,
+                   "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step vs {L2_BYTES / 1e6:.0f} MB L2)"
+                   if in_bytes > L2_BYTES else "inputs smaller than L2 (no flush)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "breakdown": breakdown,
+        "e2e": {"value": round(tokens * K / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": prob.kernels_per_step() * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.seed, sample_tokens=args.cpu_sample_tokens)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------- CPU oracle arm
+
+def cpu_baseline(w, seed, sample_tokens=16):
+    """The oracle as it stands, on a bounded sample: full preprocess and dispatch
+    (they scale with T), the MLP and combine for `sample_tokens` tokens (all
+    their routes), extrapolated to the whole batch.  Returns tokens/s."""
+    import oracle
+    import torch
+
+    oracle.build()
+    cores = os.cpu_count()
+    fmt, rmap, probs = workloads.routing_inputs(w, seed)
+    x = workloads.bf16_bits(workloads.activations(w, seed))
+    t0 = time.perf_counter()
+    cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
+    if w.cap_factor:
+        cap = oracle.capacity(oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, cap)["total_rows"], w.cap_factor)
+    pre = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, cap)
+    if w.dtype == "fp8":
+        xq, xs = oracle.quantize_fp8_rows(x)
+        yq, yp = oracle.dispatch(fmt, rmap, probs, pre, xq, cap, w.E, w.K)
+        ys, _ = oracle.dispatch(fmt, rmap, None, pre, xs, cap, w.E, w.K)
+    else:
+        yq, yp = oracle.dispatch(fmt, rmap, probs, pre, x, cap, w.E, w.K)
+        ys = None
+    t_full = time.perf_counter() - t0
+    n = min(sample_tokens, w.T)
+    toks = np.random.default_rng(0).choice(w.T, n, replace=False)
+    t1 = time.perf_counter()
+    if w.I:
+        rows = pre["row_of"][toks]
+        rows = np.unique(rows[rows >= 0])
+        experts = sorted({int(np.searchsorted(pre["offsets"], r, side="right") - 1) for r in rows})
+        w13, w2 = workloads.expert_weights(w, seed, experts=experts)
+        fmt_mlp = 0
+        w13b, w2b, s13, s2 = workloads.bf16_bits(w13), workloads.bf16_bits(w2), None, None
+        if w.dtype == "fp8":
+            fmt_mlp = 1
+            w13b, s13 = oracle.quantize_fp8_weight(w13b)
+            w2b, s2 = oracle.quantize_fp8_weight(w2b)
+        sel, off = [], [0]
+        for e in experts:
+            rr = rows[(rows >= pre["offsets"][e]) & (rows < pre["offsets"][e + 1])]
+            sel.append(rr)
+            off.append(off[-1] + len(rr))
+        sel = np.concatenate(sel)
+        ob, _ = oracle.grouped_mlp_rows(fmt_mlp, yq[sel], None if ys is None else ys[sel], w.H, w.I, len(experts),
+                                        np.array(off, np.int32), w13b, s13, w2b, s2, np.arange(len(sel)))
+        o_full = np.zeros((cap, w.H), np.uint16)
+        o_full[sel] = ob
+    else:
+        o_full = yq
+    oracle.combine(o_full, pre["row_of"][toks], yp)
+    t_sample = time.perf_counter() - t1
+    est = t_full + t_sample * (w.T / n)
+    return {"value": round(w.T / est, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"full preprocess + dispatch of {w.T} tokens ({t_full:.2f} s); grouped MLP + combine of "
+                      f"{n} sampled tokens ({t_sample:.2f} s) extrapolated x{w.T / n:.0f}"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        cpu_baseline(w, args.seed, sample_tokens=2)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(K):
+        vals.append(cpu_baseline(w, args.seed, sample_tokens=args.ref_sample_tokens))
+    wall = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": K, "warmup": W,
+            "ms_per_step": round(w.T / v * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes of the pages' workloads)",
+            "config": {"workload": w.name, "tokens": w.T, "hidden": w.H, "experts": w.E, "topk": w.K,
+                       "intermediate": w.I},
+            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"] + f"; {K} timed samples, {wall:.1f} s wall"},
+            "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mid", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    ap.add_argument("--ref-sample-tokens", type=int, default=4)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -266,6 +266,14 @@ MOE_API moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape
                            const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
                            size_t workspace_bytes, void* out_fc2, void* stream);
 
+/* Profiling hook: the next moe_grouped_mlp call made by this host thread
+ * records the three given CUDA events (cudaEvent_t passed as void*) on its
+ * stream -- before FC1, between FC1 and FC2, and after FC2 -- and then forgets
+ * them.  Pass NULLs to cancel.  Used to time the two GEMM kernels separately
+ * inside a step (TensorRT-LLM PR #16190 "Update CuTeDSL MegaMoE kernels",
+ * commit list: the microbench reports kernel-level times). */
+MOE_API moe_status moe_profile_next_grouped_mlp(void* ev_before_fc1, void* ev_after_fc1, void* ev_after_fc2);
+
 /* ------------------------------------------------- weight / row quantizers */
 
 /* bf16 [G][N][Kd] -> E4M3 codes [G][N][Kd] + fp32 scales [G][N/128][Kd/128],

@@ -90,6 +90,7 @@ _SIGNATURES = {
     "moe_grouped_mlp": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                         ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Nvfp4Globals), _P,
                         ctypes.c_size_t, _P, _P],
+    "moe_profile_next_grouped_mlp": [_P, _P, _P],
     "moe_quantize_fp8_blocks": [_P, _I64, _I64, _I64, _P, _P, _P],
     "moe_quantize_nvfp4_rows": [_P, _I64, _I64, _P, _P, _P, _P],
     "moe_ring_create": [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_P)],
@@ -282,6 +283,13 @@ def moe_combine_unpermute(handle: Handle, shape: Shape, layout: Layout, expert_o
     _check(_lib.moe_combine_unpermute(ctypes.byref(handle.c()), ctypes.byref(shape.c()), ctypes.byref(layout.c()),
                                       _ptr(expert_out), _ptr(perm_probs), _ptr(y), _stream(stream)),
            "moe_combine_unpermute")
+
+
+def moe_profile_next_grouped_mlp(ev_before_fc1, ev_after_fc1, ev_after_fc2) -> None:
+    """Record three torch.cuda.Event objects around FC1 / FC2 of the next moe_grouped_mlp call."""
+    handles = [ctypes.c_void_p(e.cuda_event) if e is not None else None
+               for e in (ev_before_fc1, ev_after_fc1, ev_after_fc2)]
+    _check(_lib.moe_profile_next_grouped_mlp(*handles), "moe_profile_next_grouped_mlp")
 
 
 def moe_quantize_fp8_blocks(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> None:

@@ -344,6 +344,8 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
       cudaSuccess)
     return e;
   const int64_t m_tiles_bound = (l.capacity + BM - 1) / BM + s.E;
+  const ProfileEvents prof = take_profile_events();
+  if (prof.before_fc1 && (e = cudaEventRecord(prof.before_fc1, st)) != cudaSuccess) return e;
 
   GemmParams p1;
   p1.offsets = h.padded_offsets;
@@ -359,6 +361,7 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
   p1.nt = (int)(s.I / 128);
   p1.nkb = (int)(s.H / BK);
   if ((e = launch_one<kFc1SwiGLU>(ta1, tb1, p1, m_tiles_bound * p1.nt, st)) != cudaSuccess) return e;
+  if (prof.after_fc1 && (e = cudaEventRecord(prof.after_fc1, st)) != cudaSuccess) return e;
 
   GemmParams p2 = p1;
   p2.out = static_cast<uint8_t*>(out_fc2);
@@ -369,7 +372,9 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
   p2.n_step = BN;
   p2.nt = (int)((s.H + BN - 1) / BN);
   p2.nkb = (int)(s.I / BK);
-  return launch_one<kFc2>(ta2, tb2, p2, m_tiles_bound * p2.nt, st);
+  if ((e = launch_one<kFc2>(ta2, tb2, p2, m_tiles_bound * p2.nt, st)) != cudaSuccess) return e;
+  if (prof.after_fc2 && (e = cudaEventRecord(prof.after_fc2, st)) != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 }  // namespace moe

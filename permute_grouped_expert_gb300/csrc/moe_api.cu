@@ -48,6 +48,18 @@ moe_status check_routing(const moe_routing* r, int64_t T) {
 }
 }  // namespace
 
+namespace {
+thread_local ProfileEvents g_profile;
+}
+
+ProfileEvents take_profile_events() {
+  ProfileEvents e = g_profile;
+  g_profile = ProfileEvents();
+  return e;
+}
+
+void set_profile_events(const ProfileEvents& ev) { g_profile = ev; }
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -214,6 +226,17 @@ moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape,
                                      static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status moe_profile_next_grouped_mlp(void* ev_before_fc1, void* ev_after_fc1, void* ev_after_fc2) {
+  ProfileEvents e;
+  e.before_fc1 = static_cast<cudaEvent_t>(ev_before_fc1);
+  e.after_fc1 = static_cast<cudaEvent_t>(ev_after_fc1);
+  e.after_fc2 = static_cast<cudaEvent_t>(ev_after_fc2);
+  if ((e.before_fc1 || e.after_fc1 || e.after_fc2) && !(e.before_fc1 && e.after_fc1 && e.after_fc2))
+    return MOE_ERR_INVALID_ARG;
+  set_profile_events(e);
+  return MOE_OK;
 }
 
 moe_status moe_quantize_fp8_blocks(const void* w, int64_t G, int64_t N, int64_t Kd, void* codes,

@@ -61,4 +61,12 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
 
 int device_sm_count();
 
+// Events the next grouped-MLP launch on this thread records (see
+// moe_profile_next_grouped_mlp); consumed and cleared by that launch.
+struct ProfileEvents {
+  cudaEvent_t before_fc1 = nullptr, after_fc1 = nullptr, after_fc2 = nullptr;
+};
+ProfileEvents take_profile_events();
+void set_profile_events(const ProfileEvents& ev);
+
 }  // namespace moe

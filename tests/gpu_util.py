@@ -78,6 +78,32 @@ def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
     return excess / rms if rms > 0 else excess
 
 
+def layer_rel_err(got_y, ref_y, ref_o_rows, weights) -> float:
+    """Tolerance measure for the layer output y = bf16(sum_k w_k * O_k): beyond
+    one bf16 step of y itself, each stored expert row O_k may differ by one
+    bf16 step of its own, which the combine carries with weight |w_k|.
+    ref_o_rows: [T, K, H] oracle expert rows (float64, 0 for dropped routes);
+    weights: [T, K] combine weights (0 for dropped routes)."""
+    got_y = np.asarray(got_y, np.float64)
+    ref_y = np.asarray(ref_y, np.float64)
+    if ref_y.size == 0:
+        return 0.0
+    carried = np.einsum("tk,tkh->th", np.abs(weights), bf16_ulp(ref_o_rows) * (ref_o_rows != 0))
+    rms = float(np.sqrt(np.mean(np.square(ref_y))))
+    excess = float(np.maximum(np.abs(got_y - ref_y) - bf16_ulp(ref_y) - carried, 0.0).max())
+    return excess / rms if rms > 0 else excess
+
+
+def gather_rows(o_full, row_of, perm_probs):
+    """Oracle expert rows and combine weights per (token, slot) for layer_rel_err."""
+    ro = np.asarray(row_of)
+    keep = ro >= 0
+    rows = np.where(keep, ro, 0)
+    o = np.asarray(o_full, np.float64)[rows] * keep[..., None]
+    wts = (np.asarray(perm_probs, np.float64)[rows] if perm_probs is not None else np.ones(ro.shape)) * keep
+    return o, wts
+
+
 def mismatch_fraction(got: np.ndarray, ref: np.ndarray) -> float:
     """Fraction of elements that are not bit-identical."""
     return float(np.mean(np.asarray(got) != np.asarray(ref))) if np.asarray(ref).size else 0.0

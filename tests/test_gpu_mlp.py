@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import workloads
-from gpu_util import bits, fill_pattern, handle_np, moe_mod, preprocess, rel_err
+from gpu_util import bits, fill_pattern, gather_rows, handle_np, layer_rel_err, moe_mod, preprocess, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,10 @@ def test_grouped_mlp_bf16_all_rows(oracle, moe, name, w):
     # whole layer vs the unpermuted per-token formulation of the oracle
     ref = oracle.layer_per_token(0, r["fmt"], r["rmap"], r["probs"], w.E, w.K, workloads.bf16_bits(r["x"]), None,
                                  w.H, w.I, w13b, None, w2b, None, np.arange(w.T))
-    assert rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(ref)) <= TOL_BF16
+    o_full = np.zeros((r["cap"], w.H), np.uint16)
+    o_full[:v] = ob
+    o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"], po)
+    assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(ref), o_rows, wts) <= TOL_BF16
 
 
 def _sampled_check(oracle, w, r, n_tokens=48, seed=0):
@@ -97,8 +100,9 @@ def _sampled_check(oracle, w, r, n_tokens=48, seed=0):
     o_full = np.zeros((r["cap"], w.H), np.uint16)
     o_full[sel] = ob
     yref = oracle.combine(o_full, pre["row_of"][toks], po)
-    assert rel_err(oracle.bf16_to_f64(bits(r["out"][torch.from_numpy(toks).cuda()])),
-                   oracle.bf16_to_f64(yref)) <= TOL_BF16
+    o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"][toks], po)
+    assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"][torch.from_numpy(toks).cuda()])),
+                         oracle.bf16_to_f64(yref), o_rows, wts) <= TOL_BF16
 
 
 def test_mid_layer_full_size_sampled(oracle, moe):
@@ -138,4 +142,5 @@ def test_overflowed_capacity_layer(oracle, moe):
     o_full = np.zeros((cap, w.H), np.uint16)
     o_full[:v] = ob
     yref = oracle.combine(o_full, pre["row_of"], po)
-    assert rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(yref)) <= TOL_BF16
+    o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"], po)
+    assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(yref), o_rows, wts) <= TOL_BF16
