@@ -102,6 +102,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------- multi-rank timing
+
+def max_over_ranks(ms: float, device=None) -> float:
+    """The slowest rank's time (all ranks get it); identity on one process."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, steps: int, ms_slowest: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (ms_slowest / 1e3)
+
+
 # ----------------------------------------------------------------- problem
 
 class Problem:
@@ -281,11 +300,7 @@ def run_ours(args, w):
         t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    total_ms = t_begin.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t_begin.elapsed_time(t_end), dev)
     ms_step = total_ms / K
 
     def mean_ms(a, b, table):
@@ -315,17 +330,13 @@ def run_ours(args, w):
             prob.out_host.copy_(prob.out, non_blocking=True)
         e2e_evs[1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e2e_evs[0].elapsed_time(e2e_evs[1])
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_evs[0].elapsed_time(e2e_evs[1]), dev)
 
     R = prob.routed_rows()
     overflow = int(prob.handle.overflow.item())
     status = int(prob.handle.status.item())
     tokens = w.T * world
-    value = tokens * K / (total_ms / 1e3)
+    value = job_throughput(w.T, world, K, total_ms)
     peaks, peak_src = load_peaks()
 
     breakdown = {
@@ -354,7 +365,8 @@ def run_ours(args, w):
     breakdown["dispatch_frac_of_hbm"] = round(breakdown["dispatch_gbs"] / peaks["hbm_gbs"], 4)
     breakdown["combine_frac_of_hbm"] = round(breakdown["combine_gbs"] / peaks["hbm_gbs"], 4)
 
-    in_bytes = prob.x.numel() * 2 + (0 if prob.identity else sum(
+    # bytes one step moves through HBM (algorithmic): L2 cannot hold them between steps
+    in_bytes = prob.dispatch_bytes(R) + prob.combine_bytes(R) + (0 if prob.identity else sum(
         t.numel() * t.element_size() for t in (prob.w13, prob.w2)))
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -363,12 +375,12 @@ def run_ours(args, w):
         "config": {"workload": w.name, "tokens": w.T, "hidden": w.H, "experts": w.E, "topk": w.K,
                    "intermediate": w.I, "pad_multiple": w.m, "routing": w.routing,
                    "capacity_factor": w.cap_factor or None, "capacity": prob.cap,
-                   "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step vs {L2_BYTES / 1e6:.0f} MB L2)"
+                   "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2)"
                    if in_bytes > L2_BYTES else "inputs smaller than L2 (no flush)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "breakdown": breakdown,
-        "e2e": {"value": round(tokens * K / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(job_throughput(w.T, world, K, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": prob.kernels_per_step() * K,
         "clocks": clk,

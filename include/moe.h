@@ -258,7 +258,7 @@ typedef struct moe_nvfp4_globals {
  *   MOE_DTYPE_NVFP4 (perm_tokens packed [cap][H/2] + perm_scales E4M3 [cap][H/16];
  *   w13 packed [E][2I][H/2] + E4M3 [E][2I][H/16]; w2 packed [E][H][I/2] + E4M3
  *   [E][H][I/16]; globals required).
- * workspace: device, >= moe_grouped_mlp_workspace_size bytes, 1024-byte aligned.
+ * workspace: device, >= moe_grouped_mlp_workspace_size bytes, 256-byte aligned.
  * out_fc2: device bf16 [cap][H]. */
 MOE_API moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
                            int32_t w_dtype, const void* perm_tokens, const void* perm_scales,

@@ -204,7 +204,7 @@ moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape,
   if (shape->I <= 0 || shape->I % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (!perm_tokens || !w13 || !w2 || !out_fc2 || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned16(perm_tokens) || !aligned16(w13) || !aligned16(w2) || !aligned16(out_fc2) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 1023u) != 0)
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return MOE_ERR_INVALID_ARG;
   switch (w_dtype) {
     case MOE_DTYPE_BF16:
