@@ -184,6 +184,30 @@ MOE_API moe_status moe_preprocess(const moe_routing* routing, const moe_shape* s
                           const moe_handle_dev* handle, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* Allocation-free variant of moe_preprocess.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory, such
+ * as a plugin running inside a host application that owns every device
+ * allocation and gives its plugins no allocator, or a latency-critical loop
+ * that sized its memory once and must not call cudaMalloc (which can
+ * synchronise the device).  It computes exactly what moe_preprocess computes,
+ * with the same kernels, but its scratch space is a fixed device array inside
+ * the library (MOE_PREPROCESS_NOALLOC_SCRATCH_BYTES, held by every GPU that
+ * loads the library until the process exits) instead of a caller workspace.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Shapes whose scratch need (moe_preprocess_workspace_size) exceeds
+ *     MOE_PREPROCESS_NOALLOC_SCRATCH_BYTES are rejected with
+ *     MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; each call clears the bytes that must start at zero on
+ *     its own stream.  Calls whose GPU work overlaps (other streams, other host
+ *     threads) race on the array and must be serialised by the caller. */
+#define MOE_PREPROCESS_NOALLOC_SCRATCH_BYTES (8u << 20)
+MOE_API moe_status moe_preprocess_noalloc(const moe_routing* routing, const moe_shape* shape,
+                                          const moe_layout* layout, const moe_handle_dev* handle, void* stream);
+
 /* --------------------------------------------------------------- dispatch */
 
 /* dispatch_with_permute ([REUSE-BUF], Summary; [ALLGATHER], Testing): for every

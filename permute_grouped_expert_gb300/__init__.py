@@ -81,6 +81,8 @@ _SIGNATURES = {
     "moe_preprocess_workspace_size": [ctypes.POINTER(_Shape), ctypes.POINTER(ctypes.c_size_t)],
     "moe_preprocess": [ctypes.POINTER(_Routing), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                        ctypes.POINTER(_HandleDev), _P, ctypes.c_size_t, _P],
+    "moe_preprocess_noalloc": [ctypes.POINTER(_Routing), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
+                               ctypes.POINTER(_HandleDev), _P],
     "moe_dispatch_permute": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                              ctypes.c_int32, _P, _P, ctypes.POINTER(_Routing), _P, _P, _P, _P],
     "moe_combine_unpermute": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
@@ -254,6 +256,15 @@ def moe_preprocess(routing: Routing, shape: Shape, layout: Layout, handle: Handl
                                ctypes.byref(handle.c()), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_preprocess")
+
+
+def moe_preprocess_noalloc(routing: Routing, shape: Shape, layout: Layout, handle: Handle, stream=None) -> None:
+    """moe_preprocess without a caller workspace: for callers that cannot
+    allocate device memory (a plugin whose host application owns all device
+    memory, a loop that must not call cudaMalloc).  Uses the library's fixed
+    scratch array; see moe_preprocess_noalloc in moe.h for its limits."""
+    _check(_lib.moe_preprocess_noalloc(ctypes.byref(routing.c()), ctypes.byref(shape.c()), ctypes.byref(layout.c()),
+                                       ctypes.byref(handle.c()), _stream(stream)), "moe_preprocess_noalloc")
 
 
 def moe_dispatch_permute(handle: Handle, shape: Shape, layout: Layout, in_dtype: int, x: torch.Tensor,

@@ -52,6 +52,8 @@ namespace {
 thread_local ProfileEvents g_profile;
 }
 
+void record_cuda_error(cudaError_t e) { cuda_fail(e); }
+
 ProfileEvents take_profile_events() {
   ProfileEvents e = g_profile;
   g_profile = ProfileEvents();

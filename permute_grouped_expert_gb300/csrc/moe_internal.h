@@ -61,6 +61,9 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
 
 int device_sm_count();
 
+// Records a CUDA error for moe_last_cuda_error() (the caller returns MOE_ERR_CUDA).
+void record_cuda_error(cudaError_t e);
+
 // Events the next grouped-MLP launch on this thread records (see
 // moe_profile_next_grouped_mlp); consumed and cleared by that launch.
 struct ProfileEvents {
