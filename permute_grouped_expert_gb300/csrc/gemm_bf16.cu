@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      bool ok = true, pending = false;
+      bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         if (!mbar_wait(&s_tempty[acc], acc_phase ^ 1, abort_flag, p.status)) {
           ok = false;
@@ -228,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; k++)
             mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          pending = true;
           mma_commit(&s_empty[stage]);
           if (++stage == kStages) {
             stage = 0;
@@ -237,13 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(&s_tfull[acc]);
-        pending = false;
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
-      if (!ok && pending) {
+      if (!ok) {
         // no MMA may still write TMEM once it is freed
         mma_commit(&s_drain);
         const uint64_t t0 = globaltimer_ns();
