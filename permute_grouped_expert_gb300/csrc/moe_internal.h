@@ -9,17 +9,22 @@
 
 namespace moe {
 
-// Preprocess tiling: tokens per tile so that one tile holds at most this many routes.
+// Preprocess tiling: about kPreTargetTiles tiles, each holding at most
+// kPreMaxEntries routes and at most kPreStageBytes bytes of routing map.
 constexpr int kPreMaxEntries = 4096;
+constexpr int kPreStageBytes = 32768;
+constexpr int kPreTargetTiles = 256;
 constexpr int kPreThreads = 256;
 constexpr int kPreWarps = kPreThreads / 32;
 
-inline int64_t pre_tokens_per_tile(int64_t K) {
-  int64_t t = kPreMaxEntries / K;
+inline int64_t pre_tokens_per_tile(int64_t T, int64_t E, int64_t K) {
+  int64_t t = (T + kPreTargetTiles - 1) / kPreTargetTiles;
+  if (t > kPreMaxEntries / K) t = kPreMaxEntries / K;
+  if (t > kPreStageBytes / E) t = kPreStageBytes / E;
   return t < 1 ? 1 : t;
 }
-inline int64_t pre_num_tiles(int64_t T, int64_t K) {
-  int64_t tpt = pre_tokens_per_tile(K);
+inline int64_t pre_num_tiles(int64_t T, int64_t E, int64_t K) {
+  int64_t tpt = pre_tokens_per_tile(T, E, K);
   int64_t n = (T + tpt - 1) / tpt;
   return n < 1 ? 1 : n;  // a zero-token call still runs one (empty) tile
 }

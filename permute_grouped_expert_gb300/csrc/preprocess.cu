@@ -72,6 +72,36 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* warp_tot, int64_t* t
   return warp_tot[warp] + incl - v;
 }
 
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* ptr) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// Copy n bytes of global memory into shared memory with the whole block:
+// 16-byte vectors over the aligned middle, single bytes at the ends.
+__device__ void stage_bytes(uint8_t* dst, const uint8_t* src, int n) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+  int head = (int)((16 - (a & 15)) & 15);
+  if (head > n) head = n;
+  const int nvec = (n - head) / 16;
+  for (int i = threadIdx.x; i < head; i += blockDim.x) dst[i] = src[i];
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + head) + i);
+    uint32_t* d = reinterpret_cast<uint32_t*>(dst + head + 16 * i);  // dst + head may be unaligned for uint4
+    if (((reinterpret_cast<uintptr_t>(d)) & 15) == 0) {
+      *reinterpret_cast<uint4*>(d) = v;
+    } else {
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 16; q++) dst[head + 16 * i + q] = (uint8_t)(w[q >> 2] >> (8 * (q & 3)));
+    }
+  }
+  for (int i = head + 16 * nvec + threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+
+constexpr int kLookbackWindow = 16;
+
 __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
   extern __shared__ __align__(16) int32_t smem[];
   const int E = (int)p.E, K = (int)p.K;
@@ -80,6 +110,7 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
   int32_t* prefix = agg + E;                   // [E] exclusive prefix of this tile
   int32_t* partial = prefix + E;               // [kPreMaxEntries] rank inside the warp's share
   int16_t* eid = reinterpret_cast<int16_t*>(partial + kPreMaxEntries);  // [kPreMaxEntries]
+  uint8_t* stage = reinterpret_cast<uint8_t*>(eid + kPreMaxEntries);    // [kPreStageBytes] routing map of the tile
   __shared__ int s_tile, s_err;
   __shared__ int64_t s_warp_tot[kPreWarps], s_total;
 
@@ -98,13 +129,20 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
   const int64_t t0 = tile * p.tokens_per_tile;
   const int64_t t1 = min64(t0 + p.tokens_per_tile, p.T);
   const int ntok = (int)max64(0, t1 - t0);
+  // stage this tile's part of the routing map in shared memory (coalesced, vectorised)
+  if (p.format == MOE_ROUTING_DENSE_I16)
+    stage_bytes(stage, static_cast<const uint8_t*>(p.map) + t0 * K * 2, ntok * K * 2);
+  else
+    stage_bytes(stage, static_cast<const uint8_t*>(p.map) + t0 * E, ntok * E);
+  __syncthreads();
+
   const int tpw = (ntok + kPreWarps - 1) / kPreWarps;  // tokens per warp
   const int wt0 = min(warp * tpw, ntok), wt1 = min(wt0 + tpw, ntok);
   int32_t* my_run = running + warp * E;
   int err = 0;
 
   if (p.format == MOE_ROUTING_DENSE_I16) {
-    const int16_t* idx = static_cast<const int16_t*>(p.map) + t0 * K;
+    const int16_t* idx = reinterpret_cast<const int16_t*>(stage);
     const int ebeg = wt0 * K, eend = wt1 * K;
     for (int base = ebeg; base < eend; base += 32) {
       const int i = base + lane;
@@ -130,13 +168,12 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
       }
     }
   } else {
-    const uint8_t* mp = static_cast<const uint8_t*>(p.map);
     for (int tl = wt0; tl < wt1; tl++) {
-      const int64_t t = t0 + tl;
+      const uint8_t* row = stage + (size_t)tl * E;
       int k_base = 0;
       for (int c = 0; c < E; c += 32) {
         const int e = c + lane;
-        const bool set = (e < E) && mp[t * E + e] != 0;
+        const bool set = (e < E) && row[e] != 0;
         const unsigned mask = __ballot_sync(0xffffffffu, set);
         const int k = k_base + __popc(mask & lanemask_lt());
         if (set) {
@@ -162,7 +199,7 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
   __syncthreads();
   if (tid == 0 && s_err) set_status(p.status, s_err);
 
-  // warp bases and tile aggregate per expert
+  // warp bases and tile aggregate per expert; publish the aggregate at once
   for (int e = tid; e < E; e += blockDim.x) {
     int s = 0;
     for (int w = 0; w < kPreWarps; w++) {
@@ -180,29 +217,51 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
     }
   }
 
-  // decoupled lookback, one expert column per thread
+  // decoupled lookback, one expert column per thread, kLookbackWindow
+  // predecessors loaded at once: stop at the nearest inclusive prefix, sum the
+  // aggregates in between, and wait (bounded) only on a tile that has not
+  // published anything yet
   if (tile > 0) {
     for (int e = tid; e < E; e += blockDim.x) {
       int64_t acc = 0;
       int64_t j = tile - 1;
       uint64_t t_start = 0;
       while (j >= 0) {
-        const uint64_t v = ld_acquire_u64(p.lookback + j * p.E + e);
-        const uint64_t flag = v & ~0xffffffffull;
-        if (flag == 0) {
+        const int n = (int)min64(kLookbackWindow, j + 1);
+        uint64_t v[kLookbackWindow];
+#pragma unroll
+        for (int q = 0; q < kLookbackWindow; q++)
+          if (q < n) v[q] = ld_relaxed_u64(p.lookback + (j - q) * p.E + e);
+        int64_t sum = 0;
+        int stop = n;
+        bool inclusive = false, not_ready = false;
+#pragma unroll
+        for (int q = 0; q < kLookbackWindow; q++) {
+          if (q >= n || inclusive || not_ready) continue;
+          const uint64_t flag = v[q] & ~0xffffffffull;
+          if (flag == 0) {
+            not_ready = true;
+            stop = q;
+          } else {
+            sum += (uint32_t)v[q];
+            if (flag == kFlagInclusive) inclusive = true;
+          }
+        }
+        acc += sum;
+        if (inclusive) break;
+        if (not_ready) {
+          j -= stop;
           const uint64_t now = globaltimer_ns();
-          if (t_start == 0) {
+          if (stop > 0 || t_start == 0) {
             t_start = now;
           } else if (now - t_start > kWaitLimitNs) {
             set_status(p.status, MOE_DEV_ERR_TIMEOUT);
             break;
           }
-          __nanosleep(64);
+          __nanosleep(32);
           continue;
         }
-        acc += (uint32_t)v;
-        if (flag == kFlagInclusive) break;
-        j--;
+        j -= n;
         t_start = 0;
       }
       prefix[e] = (int32_t)acc;
@@ -286,12 +345,12 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 }  // namespace
 
 size_t preprocess_workspace_bytes(int64_t T, int64_t E, int64_t K) {
-  const int64_t tiles = pre_num_tiles(T, K);
+  const int64_t tiles = pre_num_tiles(T, E, K);
   return 256 + align_up((size_t)tiles * E * 8, 256) + align_up((size_t)(T * K) * 2, 256);
 }
 
 PreWorkspace preprocess_workspace_carve(void* ws, int64_t T, int64_t E, int64_t K) {
-  const int64_t tiles = pre_num_tiles(T, K);
+  const int64_t tiles = pre_num_tiles(T, E, K);
   char* b = static_cast<char*>(ws);
   PreWorkspace w;
   w.tile_counter = reinterpret_cast<int32_t*>(b);
@@ -311,8 +370,8 @@ cudaError_t launch_preprocess(const moe_routing& r, const moe_shape& s, const mo
   p.K = s.K;
   p.m = l.pad_multiple;
   p.cap = l.capacity;
-  p.tokens_per_tile = pre_tokens_per_tile(s.K);
-  p.num_tiles = pre_num_tiles(s.T, s.K);
+  p.tokens_per_tile = pre_tokens_per_tile(s.T, s.E, s.K);
+  p.num_tiles = pre_num_tiles(s.T, s.E, s.K);
   p.tile_counter = ws.tile_counter;
   p.lookback = ws.lookback;
   p.route_expert = ws.route_expert;
@@ -329,11 +388,11 @@ cudaError_t launch_preprocess(const moe_routing& r, const moe_shape& s, const mo
   if ((e = cudaMemsetAsync(ws.tile_counter, 0, ws.memset_bytes, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(h.status, 0, sizeof(int32_t), st)) != cudaSuccess) return e;
 
-  const size_t smem_a = (size_t)(kPreWarps + 2) * s.E * 4 + (size_t)kPreMaxEntries * 6;
+  const size_t smem_a = (size_t)(kPreWarps + 2) * s.E * 4 + (size_t)kPreMaxEntries * 6 + kPreStageBytes;
   static bool attr_done = false;
   if (!attr_done) {
     if ((e = cudaFuncSetAttribute(pre_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)((kPreWarps + 2) * 1024 * 4 + kPreMaxEntries * 6))) != cudaSuccess)
+                                  (int)((kPreWarps + 2) * 1024 * 4 + kPreMaxEntries * 6 + kPreStageBytes))) != cudaSuccess)
       return e;
     attr_done = true;
   }
