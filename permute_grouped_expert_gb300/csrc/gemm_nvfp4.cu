@@ -1,0 +1,538 @@
+// gemm_nvfp4.cu -- persistent grouped GEMMs of the expert MLP with NVFP4
+// operands (E2M1 values, one E4M3 scale per 16 consecutive K elements, one fp32
+// global scale per tensor), shaped for decode batches: a few tokens per expert,
+// so the work is bound by streaming the expert weights from HBM.
+//
+// Follows TensorRT-LLM PR #16190 "Update CuTeDSL MegaMoE kernels" (commit
+// list: NVFP4 w3_w1_weight / w2_weight with block scales, weight_scale_2 and
+// input_scale with the epilogue alpha derived from both; decode launches sized
+// by the real token count instead of the prefill maximum).
+//
+// Orientation ("swap AB"): the weight tile is the MMA's M = 128 side and the
+// expert's tokens the N = 32 side, D^T = W . X^T, so no MMA lane is wasted on
+// the handful of rows a decode batch routes to each expert.  E2M1 x E4M3 is
+// exactly representable in f16 (at most 6 significant bits, magnitudes in
+// [2^-10, 2688]), so converter warps expand both operands to f16 in shared
+// memory exactly and tcgen05.mma kind::f16 accumulates in fp32; the two fp32
+// global scales (alpha = activation global x expert weight global) are applied
+// in the epilogue.
+//
+// One CTA per SM, 10 warps:
+//   warp 0      TMA producer: raw stages of 256 K elements (packed weights
+//               128 rows x 128 B, their scales 128 x 16 B, packed tokens 32 x 128 B,
+//               their scales 32 x 16 B), 5 stages
+//   warp 1      TMEM allocation (2 x 32 fp32 columns) and MMA issue
+//   warps 2..5  converters: E2M1 + E4M3 -> f16, written in the 128-byte swizzled
+//               K-major layout the MMA reads, 64 K elements per converted stage
+//   warps 6..9  epilogue: FC1 exchanges gate rows through shared memory, applies
+//               SwiGLU and re-encodes the intermediate to NVFP4; FC2 writes bf16.
+// Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit).
+#include "moe_internal.h"
+#include "sm100_ptx.cuh"
+#include "tensor_map.h"
+
+namespace moe {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BMW = 128;        // weight rows per tile (MMA M)
+constexpr int BNT = 32;         // tokens per tile (MMA N)
+constexpr int BKR = 256;        // K elements per raw stage
+constexpr int BKC = 64;         // K elements per converted stage
+constexpr int kRawStages = 5;
+constexpr int kCvtStages = 3;
+constexpr int kThreads = 320;
+constexpr uint32_t kRawW = BMW * (BKR / 2);        // 16 KB packed weights
+constexpr uint32_t kRawWS = BMW * (BKR / 16);      // 2 KB weight scales
+constexpr uint32_t kRawX = BNT * (BKR / 2);        // 4 KB packed tokens
+constexpr uint32_t kRawXS = BNT * (BKR / 16);      // 512 B token scales
+constexpr uint32_t kRawBytes = kRawW + kRawWS + kRawX + kRawXS;
+constexpr uint32_t kRawStride = 23552;             // kRawBytes rounded up to 1024
+constexpr uint32_t kCvtW = BMW * BKC * 2;          // 16 KB
+constexpr uint32_t kCvtX = BNT * BKC * 2;          // 4 KB
+constexpr uint32_t kCvtStride = kCvtW + kCvtX;     // 20 KB
+constexpr uint32_t kTmemCols = 64;
+constexpr int kMaxE = 1024;
+constexpr size_t kDynSmem = 1024 + (size_t)kRawStages * kRawStride + (size_t)kCvtStages * kCvtStride;
+static_assert(kRawBytes <= kRawStride, "raw stage layout");
+
+enum Mode { kFc1SwiGLU = 0, kFc2 = 1 };
+
+// Instruction descriptor: f16 x f16 -> fp32, K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+MOE_DEVICE uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+MOE_DEVICE uint32_t e4m3_pair_to_f16x2(uint32_t code) {
+  uint32_t r;
+  const uint16_t pair = (uint16_t)(code | (code << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  return r;
+}
+
+MOE_DEVICE uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+struct Fp4Params {
+  const int32_t* offsets;  // [E+1]
+  int32_t* status;
+  uint8_t* out;            // FC1: packed E2M1 [cap][I/2]; FC2: bf16 [cap][H]
+  uint8_t* out_scales;     // FC1: E4M3 [cap][I/16]
+  const float* x_global;   // [1] global scale of the token operand
+  const float* w_global;   // [E] global scale of the weights
+  const float* out_global; // FC1: [1] global scale the intermediate is encoded with
+  int64_t ld_out;          // elements per output row
+  int64_t w_rows_per_expert;
+  int64_t gate_offset;     // FC1: I
+  int E, cap, nmt, nkr;    // weight-row tiles per expert, raw stages per tile
+};
+
+struct TileInfo {
+  int e, mt, nt;
+  int64_t row0, row_end;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const int* ntt, const Fp4Params& p) {
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  TileInfo ti;
+  ti.e = lo;
+  const int local = t - prefix[lo];
+  ti.mt = local / ntt[lo];
+  ti.nt = local % ntt[lo];
+  const int64_t seg_b = min64(p.offsets[lo], p.cap);
+  ti.row_end = min64(p.offsets[lo + 1], p.cap);
+  ti.row0 = seg_b + (int64_t)ti.nt * BNT;
+  return ti;
+}
+
+// Expand one 64-element K slice of a packed row: 32 packed bytes (two 16-byte
+// chunks of a 128-byte-swizzled raw row) and 4 scale codes -> 8 swizzled
+// 16-byte chunks of f16 in the converted tile.
+__device__ __forceinline__ void convert_row(const uint8_t* raw_row_base, int r, int s, const uint8_t* scales_row,
+                                            uint8_t* cvt_row_base) {
+  const int sw = r & 7;
+  const uint4 c0 = *reinterpret_cast<const uint4*>(raw_row_base + (((2 * s) ^ sw) << 4));
+  const uint4 c1 = *reinterpret_cast<const uint4*>(raw_row_base + (((2 * s + 1) ^ sw) << 4));
+  const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales_row + 4 * s);
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int g = 0; g < 4; g++) {  // 16 elements share one scale
+    const uint32_t sh = e4m3_pair_to_f16x2((sc4 >> (8 * g)) & 0xffu);
+#pragma unroll
+    for (int h = 0; h < 2; h++) {  // one 16-byte output chunk = 8 elements = 4 packed bytes
+      const uint32_t w = words[2 * g + h];
+      uint4 o;
+      o.x = hmul2(e2m1x2_to_f16x2(w & 0xffu), sh);
+      o.y = hmul2(e2m1x2_to_f16x2((w >> 8) & 0xffu), sh);
+      o.z = hmul2(e2m1x2_to_f16x2((w >> 16) & 0xffu), sh);
+      o.w = hmul2(e2m1x2_to_f16x2(w >> 24), sh);
+      const int chunk = 2 * g + h;
+      *reinterpret_cast<uint4*>(cvt_row_base + ((chunk ^ sw) << 4)) = o;
+    }
+  }
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
+                              const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xs,
+                              Fp4Params p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t s_rfull[kRawStages], s_rempty[kRawStages], s_cfull[kCvtStages],
+      s_cempty[kCvtStages], s_tfull[2], s_tempty[2], s_xbar[2], s_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_prefix[kMaxE + 1];
+  __shared__ int s_nt[kMaxE];
+  __shared__ float s_gate[2][64][BNT + 1];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* raw = smem;
+  uint8_t* cvt = smem + (size_t)kRawStages * kRawStride;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &s_abort;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kRawStages; s++) {
+      mbar_init(&s_rfull[s], 1);
+      mbar_init(&s_rempty[s], 4);
+    }
+    for (int s = 0; s < kCvtStages; s++) {
+      mbar_init(&s_cfull[s], 4);
+      mbar_init(&s_cempty[s], 1);
+    }
+    for (int a = 0; a < 2; a++) {
+      mbar_init(&s_tfull[a], 1);
+      mbar_init(&s_tempty[a], 4);
+      mbar_init(&s_xbar[a], 4);
+    }
+    mbar_init(&s_drain, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_ws);
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_xs);
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+  if (warp == 0) {
+    const int per = (p.E + 31) / 32;
+    int local = 0;
+    for (int j = 0; j < per; j++) {
+      const int e = lane * per + j;
+      if (e < p.E) {
+        const int64_t b = min64(p.offsets[e], p.cap), en = min64(p.offsets[e + 1], p.cap);
+        const int n = en > b ? (int)((en - b + BNT - 1) / BNT) : 0;
+        s_nt[e] = n;
+        local += n;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per; j++) {
+      const int e = lane * per + j;
+      if (e < p.E) {
+        s_prefix[e] = run * p.nmt;
+        run += s_nt[e];
+      }
+    }
+    if (lane == 31) s_prefix[p.E] = incl * p.nmt;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+  const int total = s_prefix[p.E];
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_parity[kRawStages];
+      bool issued[kRawStages];
+      for (int s = 0; s < kRawStages; s++) issued[s] = false;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
+        const int64_t wbase = (int64_t)ti.e * p.w_rows_per_expert;
+        for (int kr = 0; kr < p.nkr; kr++) {
+          if (!mbar_wait(&s_rempty[stage], phase ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = raw + (size_t)stage * kRawStride;
+          mbar_arrive_expect_tx(&s_rfull[stage], kRawBytes);
+          const int32_t cx = kr * (BKR / 2), cs = kr * (BKR / 16);
+          if (kMode == kFc1SwiGLU) {
+            const int64_t up = wbase + (int64_t)ti.mt * 64, gate = up + p.gate_offset;
+            tma_load_2d(st, &tm_w, cx, (int32_t)up, &s_rfull[stage]);
+            tma_load_2d(st + kRawW / 2, &tm_w, cx, (int32_t)gate, &s_rfull[stage]);
+            tma_load_2d(st + kRawW, &tm_ws, cs, (int32_t)up, &s_rfull[stage]);
+            tma_load_2d(st + kRawW + kRawWS / 2, &tm_ws, cs, (int32_t)gate, &s_rfull[stage]);
+          } else {
+            const int64_t r0 = wbase + (int64_t)ti.mt * BMW;
+            tma_load_2d(st, &tm_w, cx, (int32_t)r0, &s_rfull[stage]);
+            tma_load_2d(st + kRawW, &tm_ws, cs, (int32_t)r0, &s_rfull[stage]);
+          }
+          tma_load_2d(st + kRawW + kRawWS, &tm_x, cx, (int32_t)ti.row0, &s_rfull[stage]);
+          tma_load_2d(st + kRawW + kRawWS + kRawX, &tm_xs, cs, (int32_t)ti.row0, &s_rfull[stage]);
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == kRawStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kRawStages; s++) {
+          if (!issued[s]) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&s_rfull[s], issued_parity[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BMW, BNT);
+      int cst = 0, acc = 0;
+      uint32_t cphase = 0, acc_phase = 0;
+      bool ok = true;
+      const int nsub = p.nkr * (BKR / BKC);
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait(&s_tempty[acc], acc_phase ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BNT);
+        for (int ks = 0; ks < nsub; ks++) {
+          if (!mbar_wait(&s_cfull[cst], cphase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t cw = smem_u32(cvt + (size_t)cst * kCvtStride);
+          const uint64_t wdesc = smem_desc_sw128(cw);
+          const uint64_t xdesc = smem_desc_sw128(cw + kCvtW);
+#pragma unroll
+          for (int k = 0; k < BKC / 16; k++)
+            mma_bf16(d_tmem, wdesc + 2 * k, xdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+          mma_commit(&s_cempty[cst]);
+          if (++cst == kCvtStages) {
+            cst = 0;
+            cphase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&s_tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (!ok) {
+        mma_commit(&s_drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&s_drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------- converters
+    const int r = threadIdx.x - 64;  // weight row 0..127; rows < 32 also convert a token row
+    int rst = 0, cst = 0;
+    uint32_t rphase = 0, cphase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int kr = 0; kr < p.nkr && ok; kr++) {
+        int w_ok = 0;
+        if (lane == 0) w_ok = mbar_wait(&s_rfull[rst], rphase, abort_flag, p.status) ? 1 : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        const uint8_t* st = raw + (size_t)rst * kRawStride;
+        for (int s = 0; s < BKR / BKC; s++) {
+          int c_ok = 0;
+          if (lane == 0) c_ok = mbar_wait(&s_cempty[cst], cphase ^ 1, abort_flag, p.status) ? 1 : 0;
+          c_ok = __shfl_sync(0xffffffffu, c_ok, 0);
+          if (!c_ok) {
+            ok = false;
+            break;
+          }
+          uint8_t* cs = cvt + (size_t)cst * kCvtStride;
+          convert_row(st + r * (BKR / 2), r, s, st + kRawW + r * (BKR / 16), cs + r * (BKC * 2));
+          if (r < BNT)
+            convert_row(st + kRawW + kRawWS + r * (BKR / 2), r, s, st + kRawW + kRawWS + kRawX + r * (BKR / 16),
+                        cs + kCvtW + r * (BKC * 2));
+          // make the generic-proxy stores visible to the tensor cores, then publish
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_cfull[cst]);
+          if (++cst == kCvtStages) {
+            cst = 0;
+            cphase ^= 1;
+          }
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_rempty[rst]);
+        if (++rst == kRawStages) {
+          rst = 0;
+          rphase ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;             // TMEM lane quarter: weight rows 32q .. 32q+31
+    const int wr = 32 * q + lane;       // weight row of this thread within the tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int tile_iter = 0;
+    const float xg = *p.x_global;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, tile_iter++) {
+      const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(&s_tfull[acc], acc_phase, abort_flag, p.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      float v[32];
+      tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BNT), v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+      const float alpha = xg * p.w_global[ti.e];
+      if (kMode == kFc2) {
+        const int64_t col = (int64_t)ti.mt * BMW + wr;
+        uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
+#pragma unroll
+        for (int j = 0; j < BNT; j++) {
+          const int64_t row = ti.row0 + j;
+          if (row < ti.row_end) out[row * p.ld_out + col] = (uint16_t)float_to_bf16_bits(alpha * v[j]);
+        }
+      } else {
+        // rows 0..63 of the tile are up (w3), rows 64..127 gate (w1) of columns mt*64 + (wr & 63)
+        float (*gbuf)[BNT + 1] = s_gate[tile_iter & 1];
+        if (q >= 2) {
+#pragma unroll
+          for (int j = 0; j < BNT; j++) gbuf[wr - 64][j] = alpha * v[j];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_xbar[tile_iter & 1]);
+        int x_ok = 0;
+        if (lane == 0) x_ok = mbar_wait(&s_xbar[tile_iter & 1], (tile_iter >> 1) & 1, abort_flag, p.status) ? 1 : 0;
+        x_ok = __shfl_sync(0xffffffffu, x_ok, 0);
+        if (!x_ok) break;
+        if (q < 2) {
+          const float g2 = *p.out_global;
+          const int64_t col = (int64_t)ti.mt * 64 + wr;  // intermediate column of this thread
+#pragma unroll 4
+          for (int j = 0; j < BNT; j++) {
+            const float gt = gbuf[wr][j];
+            const float a = gt / (1.0f + __expf(-gt)) * (alpha * v[j]);
+            // NVFP4 block = 16 consecutive columns = 16 consecutive lanes
+            float amax = fabsf(a);
+#pragma unroll
+            for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+            const uint32_t scode = e4m3x2(__fdiv_rn(amax, 6.0f * g2), 0.0f) & 0xffu;
+            const float denom = e4m3_to_float(scode) * g2;
+            const float partner = __shfl_xor_sync(0xffffffffu, a, 1);
+            const int64_t row = ti.row0 + j;
+            if (row < ti.row_end) {
+              if ((lane & 1) == 0) {
+                const uint32_t b = (denom == 0.0f) ? 0u : e2m1x2(__fdiv_rn(a, denom), __fdiv_rn(partner, denom));
+                p.out[row * (p.ld_out / 2) + col / 2] = (uint8_t)b;
+              }
+              if ((lane & 15) == 0) p.out_scales[row * (p.ld_out / 16) + col / 16] = (uint8_t)scode;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int kMode>
+cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tws, const CUtensorMap& tx, const CUtensorMap& txs,
+                       const Fp4Params& p, int64_t max_tiles, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<kMode>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  int64_t grid = device_sm_count();
+  if (grid > max_tiles) grid = max_tiles;
+  if (grid < 1) grid = 1;
+  grouped_gemm_nvfp4_kernel<kMode><<<(unsigned)grid, kThreads, kDynSmem, st>>>(tw, tws, tx, txs, p);
+  return cudaGetLastError();
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                                     const void* perm_packed, const void* perm_scales, const void* w13,
+                                     const void* w13_scales, const void* w2, const void* w2_scales,
+                                     const moe_nvfp4_globals& g, void* workspace, void* out_fc2, cudaStream_t st) {
+  if (l.capacity == 0) return cudaSuccess;
+  if (s.E > kMaxE || s.H % BKR != 0 || s.I % BKR != 0) return cudaErrorNotSupported;
+  const uint64_t cap = (uint64_t)l.capacity;
+  uint8_t* act = static_cast<uint8_t*>(workspace);
+  uint8_t* act_scales = act + round_up(cap * s.I / 2, 1024);
+  CUtensorMap w1, w1s, x1, x1s, w2m, w2s, x2, x2s;
+  cudaError_t e;
+  const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  const auto NO = CU_TENSOR_MAP_SWIZZLE_NONE;
+  const uint64_t rows13 = (uint64_t)s.E * 2 * s.I, rows2 = (uint64_t)s.E * s.H;
+  if ((e = make_tensor_map_2d(&w1, w13, U8, 1, rows13, s.H / 2, 64, BKR / 2, SW)) != cudaSuccess) return e;
+  if ((e = make_tensor_map_2d(&w1s, w13_scales, U8, 1, rows13, s.H / 16, 64, BKR / 16, NO)) != cudaSuccess) return e;
+  if ((e = make_tensor_map_2d(&x1, perm_packed, U8, 1, cap, s.H / 2, BNT, BKR / 2, SW)) != cudaSuccess) return e;
+  if ((e = make_tensor_map_2d(&x1s, perm_scales, U8, 1, cap, s.H / 16, BNT, BKR / 16, NO)) != cudaSuccess) return e;
+  if ((e = make_tensor_map_2d(&w2m, w2, U8, 1, rows2, s.I / 2, BMW, BKR / 2, SW)) != cudaSuccess) return e;
+  if ((e = make_tensor_map_2d(&w2s, w2_scales, U8, 1, rows2, s.I / 16, BMW, BKR / 16, NO)) != cudaSuccess) return e;
+  if ((e = make_tensor_map_2d(&x2, act, U8, 1, cap, s.I / 2, BNT, BKR / 2, SW)) != cudaSuccess) return e;
+  if ((e = make_tensor_map_2d(&x2s, act_scales, U8, 1, cap, s.I / 16, BNT, BKR / 16, NO)) != cudaSuccess) return e;
+  const int64_t n_tiles_bound = (l.capacity + BNT - 1) / BNT + s.E;
+  const ProfileEvents prof = take_profile_events();
+  if (prof.before_fc1 && (e = cudaEventRecord(prof.before_fc1, st)) != cudaSuccess) return e;
+
+  Fp4Params p1;
+  p1.offsets = h.padded_offsets;
+  p1.status = h.status;
+  p1.out = act;
+  p1.out_scales = act_scales;
+  p1.x_global = g.fc1_input_scale;
+  p1.w_global = g.w13_scale_2;
+  p1.out_global = g.fc2_input_scale;
+  p1.ld_out = s.I;
+  p1.w_rows_per_expert = 2 * s.I;
+  p1.gate_offset = s.I;
+  p1.E = (int)s.E;
+  p1.cap = (int)l.capacity;
+  p1.nmt = (int)(s.I / 64);
+  p1.nkr = (int)(s.H / BKR);
+  if ((e = launch_one<kFc1SwiGLU>(w1, w1s, x1, x1s, p1, n_tiles_bound * p1.nmt, st)) != cudaSuccess) return e;
+  if (prof.after_fc1 && (e = cudaEventRecord(prof.after_fc1, st)) != cudaSuccess) return e;
+
+  Fp4Params p2 = p1;
+  p2.out = static_cast<uint8_t*>(out_fc2);
+  p2.out_scales = nullptr;
+  p2.x_global = g.fc2_input_scale;
+  p2.w_global = g.w2_scale_2;
+  p2.out_global = nullptr;
+  p2.ld_out = s.H;
+  p2.w_rows_per_expert = s.H;
+  p2.gate_offset = 0;
+  p2.nmt = (int)(s.H / BMW);
+  p2.nkr = (int)(s.I / BKR);
+  if ((e = launch_one<kFc2>(w2m, w2s, x2, x2s, p2, n_tiles_bound * p2.nmt, st)) != cudaSuccess) return e;
+  if (prof.after_fc2 && (e = cudaEventRecord(prof.after_fc2, st)) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+}  // namespace moe

@@ -13,6 +13,11 @@ cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, 
                                    const void* w13_scales, const void* w2, const void* w2_scales, void* workspace,
                                    void* out_fc2, cudaStream_t st);
 
+cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                                     const void* perm_packed, const void* perm_scales, const void* w13,
+                                     const void* w13_scales, const void* w2, const void* w2_scales,
+                                     const moe_nvfp4_globals& g, void* workspace, void* out_fc2, cudaStream_t st);
+
 namespace {
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 }  // namespace
@@ -35,13 +40,15 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                const void* w13, const void* w13_scales, const void* w2,
                                const void* w2_scales, const moe_nvfp4_globals* globals,
                                void* workspace, void* out_fc2, cudaStream_t st) {
-  (void)globals;
   switch (w_dtype) {
     case MOE_DTYPE_BF16:
       return launch_grouped_mlp_bf16(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
     case MOE_DTYPE_FP8_E4M3_B128:
       return launch_grouped_mlp_fp8(h, s, l, perm_tokens, perm_scales, w13, w13_scales, w2, w2_scales, workspace,
                                     out_fc2, st);
+    case MOE_DTYPE_NVFP4:
+      return launch_grouped_mlp_nvfp4(h, s, l, perm_tokens, perm_scales, w13, w13_scales, w2, w2_scales, *globals,
+                                      workspace, out_fc2, st);
     default:
       return cudaErrorNotSupported;
   }
