@@ -17,14 +17,16 @@
 // global scales (alpha = activation global x expert weight global) are applied
 // in the epilogue.
 //
-// One CTA per SM, 10 warps:
+// One CTA per SM, 14 warps:
 //   warp 0      TMA producer: raw stages of 256 K elements (packed weights
 //               128 rows x 128 B, their scales 128 x 16 B, packed tokens 32 x 128 B,
 //               their scales 32 x 16 B), 5 stages
 //   warp 1      TMEM allocation (2 x 32 fp32 columns) and MMA issue
-//   warps 2..5  converters: E2M1 + E4M3 -> f16, written in the 128-byte swizzled
-//               K-major layout the MMA reads, 64 K elements per converted stage
-//   warps 6..9  epilogue: FC1 exchanges gate rows through shared memory, applies
+//   warps 2..9  converters: E2M1 + E4M3 -> f16, written in the 128-byte swizzled
+//               K-major layout the MMA reads, 64 K elements per converted stage;
+//               each thread expands half a weight row (plus, for 64 threads, half
+//               a token row)
+//   warps 10..13 epilogue: FC1 exchanges gate rows through shared memory, applies
 //               SwiGLU and re-encodes the intermediate to NVFP4; FC2 writes bf16.
 // Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit).
 #include "moe_internal.h"
@@ -43,7 +45,8 @@ constexpr int BKR = 256;        // K elements per raw stage
 constexpr int BKC = 64;         // K elements per converted stage
 constexpr int kRawStages = 5;
 constexpr int kCvtStages = 3;
-constexpr int kThreads = 320;
+constexpr int kCvtWarps = 8;
+constexpr int kThreads = 64 + 32 * kCvtWarps + 128;
 constexpr uint32_t kRawW = BMW * (BKR / 2);        // 16 KB packed weights
 constexpr uint32_t kRawWS = BMW * (BKR / 16);      // 2 KB weight scales
 constexpr uint32_t kRawX = BNT * (BKR / 2);        // 4 KB packed tokens
@@ -123,28 +126,27 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
   return ti;
 }
 
-// Expand one 64-element K slice of a packed row: 32 packed bytes (two 16-byte
-// chunks of a 128-byte-swizzled raw row) and 4 scale codes -> 8 swizzled
-// 16-byte chunks of f16 in the converted tile.
-__device__ __forceinline__ void convert_row(const uint8_t* raw_row_base, int r, int s, const uint8_t* scales_row,
-                                            uint8_t* cvt_row_base) {
+// Expand half of one 64-element K slice of a packed row: 32 elements = one
+// 16-byte chunk of the 128-byte-swizzled raw row (K slice s, half h) plus its
+// two scale codes -> four swizzled 16-byte chunks of f16 in the converted tile.
+__device__ __forceinline__ void convert_half_row(const uint8_t* raw_row_base, int r, int s, int h,
+                                                 const uint8_t* scales_row, uint8_t* cvt_row_base) {
   const int sw = r & 7;
-  const uint4 c0 = *reinterpret_cast<const uint4*>(raw_row_base + (((2 * s) ^ sw) << 4));
-  const uint4 c1 = *reinterpret_cast<const uint4*>(raw_row_base + (((2 * s + 1) ^ sw) << 4));
-  const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales_row + 4 * s);
-  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const uint4 c = *reinterpret_cast<const uint4*>(raw_row_base + (((2 * s + h) ^ sw) << 4));
+  const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(scales_row + 4 * s + 2 * h);
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-  for (int g = 0; g < 4; g++) {  // 16 elements share one scale
-    const uint32_t sh = e4m3_pair_to_f16x2((sc4 >> (8 * g)) & 0xffu);
+  for (int g = 0; g < 2; g++) {  // 16 elements share one scale
+    const uint32_t sh = e4m3_pair_to_f16x2((sc2 >> (8 * g)) & 0xffu);
 #pragma unroll
-    for (int h = 0; h < 2; h++) {  // one 16-byte output chunk = 8 elements = 4 packed bytes
-      const uint32_t w = words[2 * g + h];
+    for (int i = 0; i < 2; i++) {  // one 16-byte output chunk = 8 elements = 4 packed bytes
+      const uint32_t w = words[2 * g + i];
       uint4 o;
       o.x = hmul2(e2m1x2_to_f16x2(w & 0xffu), sh);
       o.y = hmul2(e2m1x2_to_f16x2((w >> 8) & 0xffu), sh);
       o.z = hmul2(e2m1x2_to_f16x2((w >> 16) & 0xffu), sh);
       o.w = hmul2(e2m1x2_to_f16x2(w >> 24), sh);
-      const int chunk = 2 * g + h;
+      const int chunk = 4 * h + 2 * g + i;
       *reinterpret_cast<uint4*>(cvt_row_base + ((chunk ^ sw) << 4)) = o;
     }
   }
@@ -174,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     for (int s = 0; s < kRawStages; s++) {
       mbar_init(&s_rfull[s], 1);
-      mbar_init(&s_rempty[s], 4);
+      mbar_init(&s_rempty[s], kCvtWarps);
     }
     for (int s = 0; s < kCvtStages; s++) {
-      mbar_init(&s_cfull[s], 4);
+      mbar_init(&s_cfull[s], kCvtWarps);
       mbar_init(&s_cempty[s], 1);
     }
     for (int a = 0; a < 2; a++) {
@@ -324,9 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kCvtWarps) {
     // ---------------------------------------------------------- converters
-    const int r = threadIdx.x - 64;  // weight row 0..127; rows < 32 also convert a token row
+    const int c = threadIdx.x - 64;  // 0..255: weight row c & 127, half c >> 7
+    const int wrow = c & 127, whalf = c >> 7;
+    const int xrow = c & 31, xhalf = (c >> 5) & 1;  // token half-rows for c < 64
     int rst = 0, cst = 0;
     uint32_t rphase = 0, cphase = 0;
     bool ok = true;
@@ -349,10 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* cs = cvt + (size_t)cst * kCvtStride;
-          convert_row(st + r * (BKR / 2), r, s, st + kRawW + r * (BKR / 16), cs + r * (BKC * 2));
-          if (r < BNT)
-            convert_row(st + kRawW + kRawWS + r * (BKR / 2), r, s, st + kRawW + kRawWS + kRawX + r * (BKR / 16),
-                        cs + kCvtW + r * (BKC * 2));
+          convert_half_row(st + wrow * (BKR / 2), wrow, s, whalf, st + kRawW + wrow * (BKR / 16),
+                           cs + wrow * (BKC * 2));
+          if (c < 2 * BNT)
+            convert_half_row(st + kRawW + kRawWS + xrow * (BKR / 2), xrow, s, xhalf,
+                             st + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2));
           // make the generic-proxy stores visible to the tensor cores, then publish
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();

@@ -8,6 +8,10 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
                                     const void* perm_tokens, const void* w13, const void* w2, void* act,
                                     void* out_fc2, cudaStream_t st);
 
+cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                                         const void* perm_tokens, const void* w13, const void* w2, void* act,
+                                         void* out_fc2, cudaStream_t st);
+
 cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                    const void* perm_codes, const void* perm_scales, const void* w13,
                                    const void* w13_scales, const void* w2, const void* w2_scales, void* workspace,
@@ -19,6 +23,7 @@ cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s
                                      const moe_nvfp4_globals& g, void* workspace, void* out_fc2, cudaStream_t st);
 
 namespace {
+constexpr int64_t kPairMinRows = 1024;
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 }  // namespace
 
@@ -42,6 +47,10 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                void* workspace, void* out_fc2, cudaStream_t st) {
   switch (w_dtype) {
     case MOE_DTYPE_BF16:
+      // Large problems run each MMA across an SM pair (256-row tiles); small ones
+      // keep 128-row tiles on single SMs so that fewer rows go to waste.
+      if (l.capacity >= kPairMinRows)
+        return launch_grouped_mlp_bf16_pair(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
       return launch_grouped_mlp_bf16(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
     case MOE_DTYPE_FP8_E4M3_B128:
       return launch_grouped_mlp_fp8(h, s, l, perm_tokens, perm_scales, w13, w13_scales, w2, w2_scales, workspace,
