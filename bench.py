@@ -195,6 +195,7 @@ class Problem:
                 self.x_scales = g1
                 self.globals = moe.Nvfp4Globals(g1, torch.tensor([0.01], device=dev), g13, g2)
             del w13, w2
+            torch.cuda.empty_cache()  # release the bf16 weight temporaries
             self.act_ws = torch.empty(moe.moe_grouped_mlp_workspace_size(self.shape, self.layout, self.w_dtype),
                                       dtype=torch.uint8, device=dev)
             self.o = torch.empty(cap, w.H, dtype=torch.bfloat16, device=dev)
@@ -490,10 +491,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--ref-sample-tokens", type=int, default=4)
+    ap.add_argument("--set", action="append", default=[], metavar="FIELD=INT",
+                    help="shrink the workload for profiling captures, e.g. --set E=32 --set T=1024")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = workloads.WORKLOADS[args.workload]
+    if args.set:
+        changes = {k: int(v) for k, v in (kv.split("=", 1) for kv in args.set)}
+        w = workloads.scaled(w, name=w.name + "+" + ",".join(args.set), **changes)
     if args.impl == "reference":
         run_reference(args, w)
     else:

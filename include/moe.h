@@ -298,6 +298,17 @@ MOE_API moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape
  * commit list: the microbench reports kernel-level times). */
 MOE_API moe_status moe_profile_next_grouped_mlp(void* ev_before_fc1, void* ev_after_fc1, void* ev_after_fc2);
 
+/* Testing hook for the failure path of the bounded inter-CTA waits: runs
+ * moe_preprocess with tile `silent_tile` (>= 0) withholding its lookback
+ * publication, so every later tile's bounded wait runs out (after about 2 s),
+ * MOE_DEV_ERR_TIMEOUT is set in handle->status and the kernel returns; no
+ * kernel traps and the context stays usable.  The handle's other outputs of
+ * that call are not valid.  Not for production use. */
+MOE_API moe_status moe_debug_preprocess_silent_tile(const moe_routing* routing, const moe_shape* shape,
+                                                    const moe_layout* layout, const moe_handle_dev* handle,
+                                                    void* workspace, size_t workspace_bytes, int64_t silent_tile,
+                                                    void* stream);
+
 /* ------------------------------------------------- weight / row quantizers */
 
 /* bf16 [G][N][Kd] -> E4M3 codes [G][N][Kd] + fp32 scales [G][N/128][Kd/128],

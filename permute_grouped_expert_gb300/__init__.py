@@ -93,6 +93,8 @@ _SIGNATURES = {
                         ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Nvfp4Globals), _P,
                         ctypes.c_size_t, _P, _P],
     "moe_profile_next_grouped_mlp": [_P, _P, _P],
+    "moe_debug_preprocess_silent_tile": [ctypes.POINTER(_Routing), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
+                                         ctypes.POINTER(_HandleDev), _P, ctypes.c_size_t, ctypes.c_int64, _P],
     "moe_quantize_fp8_blocks": [_P, _I64, _I64, _I64, _P, _P, _P],
     "moe_quantize_nvfp4_rows": [_P, _I64, _I64, _P, _P, _P, _P],
     "moe_ring_create": [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_P)],
@@ -301,6 +303,15 @@ def moe_profile_next_grouped_mlp(ev_before_fc1, ev_after_fc1, ev_after_fc2) -> N
     handles = [ctypes.c_void_p(e.cuda_event) if e is not None else None
                for e in (ev_before_fc1, ev_after_fc1, ev_after_fc2)]
     _check(_lib.moe_profile_next_grouped_mlp(*handles), "moe_profile_next_grouped_mlp")
+
+
+def moe_debug_preprocess_silent_tile(routing: Routing, shape: Shape, layout: Layout, handle: Handle,
+                                     workspace: torch.Tensor, silent_tile: int, stream=None) -> None:
+    """Testing hook: preprocess with one tile withholding its lookback publication (see moe.h)."""
+    _check(_lib.moe_debug_preprocess_silent_tile(ctypes.byref(routing.c()), ctypes.byref(shape.c()),
+                                                 ctypes.byref(layout.c()), ctypes.byref(handle.c()), _ptr(workspace),
+                                                 workspace.numel() * workspace.element_size(), silent_tile,
+                                                 _stream(stream)), "moe_debug_preprocess_silent_tile")
 
 
 def moe_quantize_fp8_blocks(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> None:

@@ -141,6 +141,22 @@ moe_status moe_preprocess(const moe_routing* routing, const moe_shape* shape, co
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+moe_status moe_debug_preprocess_silent_tile(const moe_routing* routing, const moe_shape* shape,
+                                            const moe_layout* layout, const moe_handle_dev* handle, void* workspace,
+                                            size_t workspace_bytes, int64_t silent_tile, void* stream) {
+  MOE_TRY(check_shape(shape, false));
+  MOE_TRY(check_routing(routing, shape->T));
+  MOE_TRY(check_layout(layout));
+  MOE_TRY(check_handle(handle));
+  if (!workspace || !aligned16(workspace) || silent_tile < 0) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < preprocess_workspace_bytes(shape->T, shape->E, shape->K))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const PreWorkspace ws = preprocess_workspace_carve(workspace, shape->T, shape->E, shape->K);
+  cudaError_t e = launch_preprocess(*routing, *shape, *layout, *handle, ws, static_cast<cudaStream_t>(stream),
+                                    silent_tile);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
 moe_status moe_dispatch_permute(const moe_handle_dev* handle, const moe_shape* shape,
                                 const moe_layout* layout, int32_t in_dtype, const void* x,
                                 const void* x_scales, const moe_routing* routing, void* out_tokens,

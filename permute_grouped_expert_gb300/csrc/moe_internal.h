@@ -40,7 +40,8 @@ size_t preprocess_workspace_bytes(int64_t T, int64_t E, int64_t K);
 PreWorkspace preprocess_workspace_carve(void* ws, int64_t T, int64_t E, int64_t K);
 
 cudaError_t launch_preprocess(const moe_routing& r, const moe_shape& s, const moe_layout& l,
-                              const moe_handle_dev& h, const PreWorkspace& ws, cudaStream_t st);
+                              const moe_handle_dev& h, const PreWorkspace& ws, cudaStream_t st,
+                              int64_t silent_tile = -1);
 
 cudaError_t launch_dispatch(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                             int32_t in_dtype, const void* x, const void* x_scales,

@@ -46,6 +46,7 @@ struct PreParams {
   int32_t* total_rows;
   int32_t* overflow;
   int32_t* status;
+  int64_t silent_tile;  // testing hook: this tile never publishes its lookback words (-1: none)
 };
 
 // Exclusive scan of one int64 per thread across the block (kPreThreads threads).
@@ -209,7 +210,9 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
     }
     agg[e] = s;
     uint64_t* word = p.lookback + tile * p.E + e;
-    if (tile == 0) {
+    if (tile == p.silent_tile) {
+      // testing hook: successors find nothing published and their bounded wait runs out
+    } else if (tile == 0) {
       prefix[e] = 0;
       st_release_u64(word, kFlagInclusive | (uint32_t)s);
     } else {
@@ -265,7 +268,8 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
         t_start = 0;
       }
       prefix[e] = (int32_t)acc;
-      st_release_u64(p.lookback + tile * p.E + e, kFlagInclusive | (uint32_t)(acc + agg[e]));
+      if (tile != p.silent_tile)
+        st_release_u64(p.lookback + tile * p.E + e, kFlagInclusive | (uint32_t)(acc + agg[e]));
     }
   }
   __syncthreads();
@@ -361,8 +365,9 @@ PreWorkspace preprocess_workspace_carve(void* ws, int64_t T, int64_t E, int64_t 
 }
 
 cudaError_t launch_preprocess(const moe_routing& r, const moe_shape& s, const moe_layout& l,
-                              const moe_handle_dev& h, const PreWorkspace& ws, cudaStream_t st) {
+                              const moe_handle_dev& h, const PreWorkspace& ws, cudaStream_t st, int64_t silent_tile) {
   PreParams p;
+  p.silent_tile = silent_tile;
   p.format = r.format;
   p.map = r.map;
   p.T = s.T;
