@@ -75,8 +75,8 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
   TileInfo ti;
   ti.e = lo;
   const int local = t - prefix[lo];
-  ti.n = local / mt[lo];
-  ti.m = local % mt[lo];
+  ti.m = local / p.nt;
+  ti.n = local % p.nt;
   const int64_t seg_b = min64(p.offsets[lo], p.cap);
   ti.row_end = min64(p.offsets[lo + 1], p.cap);
   ti.row0 = seg_b + (int64_t)ti.m * (2 * BMC);

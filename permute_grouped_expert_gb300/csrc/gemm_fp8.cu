@@ -294,11 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; j++) acc[j] = 0.0f;
+      // scales of the next K block are loaded while this one is folded in
       float sa_next = row_in ? __ldg(arow) : 0.0f;
+      float sb0_next = __ldg(bs0), sb1_next = __ldg(bs1);
       for (int kb = 0; kb < p.nkb; kb++) {
-        const float sa = sa_next;
-        const float sb0 = __ldg(bs0 + kb), sb1 = __ldg(bs1 + kb);
-        if (kb + 1 < p.nkb) sa_next = row_in ? __ldg(arow + kb + 1) : 0.0f;
+        const float sa = sa_next, sb0 = sb0_next, sb1 = sb1_next;
+        if (kb + 1 < p.nkb) {
+          sa_next = row_in ? __ldg(arow + kb + 1) : 0.0f;
+          sb0_next = __ldg(bs0 + kb + 1);
+          sb1_next = __ldg(bs1 + kb + 1);
+        }
         int w_ok = 0;
         if (lane == 0) w_ok = mbar_wait(&s_pfull[buf], buf_phase, abort_flag, p.status) ? 1 : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
