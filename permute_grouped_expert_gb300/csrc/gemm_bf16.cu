@@ -15,8 +15,9 @@
 //               tcgen05.commit frees ring stages and publishes accumulators.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
 //               SwiGLU (FC1) or plain bf16 conversion (FC2), 16-byte stores.
-// Tiles are (expert, N tile, M tile), M innermost so that CTAs running side by
-// side share the weight tile in L2.  Group sizes live only on the device: each
+// Tiles are (expert, M tile, N tile), N innermost so that CTAs running side by
+// side share the activation tile in L2 (and the N tiles of one M tile finish
+// together).  Group sizes live only on the device: each
 // CTA derives the tile list from the padded offsets, so the launch shape does
 // not depend on the routing and the kernel can be captured in a CUDA graph.
 // Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit).
@@ -71,8 +72,8 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
   TileInfo ti;
   ti.e = lo;
   const int local = t - prefix[lo];
-  ti.n = local / mt[lo];
-  ti.m = local % mt[lo];
+  ti.m = local / p.nt;
+  ti.n = local % p.nt;
   const int64_t seg_b = min64(p.offsets[lo], p.cap);
   ti.row_end = min64(p.offsets[lo + 1], p.cap);
   ti.row0 = seg_b + (int64_t)ti.m * BM;

@@ -23,7 +23,7 @@ cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s
                                      const moe_nvfp4_globals& g, void* workspace, void* out_fc2, cudaStream_t st);
 
 namespace {
-constexpr int64_t kPairMinRows = 1024;
+constexpr int64_t kPairMinRowsPerExpert = 2048;
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 }  // namespace
 
@@ -47,9 +47,10 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                void* workspace, void* out_fc2, cudaStream_t st) {
   switch (w_dtype) {
     case MOE_DTYPE_BF16:
-      // Large problems run each MMA across an SM pair (256-row tiles); small ones
-      // keep 128-row tiles on single SMs so that fewer rows go to waste.
-      if (l.capacity >= kPairMinRows)
+      // Experts with thousands of rows run each MMA across an SM pair (256-row
+      // tiles); otherwise 128-row tiles on single SMs waste fewer rows on the
+      // ragged last tile of each expert segment.
+      if (l.capacity >= kPairMinRowsPerExpert * s.E)
         return launch_grouped_mlp_bf16_pair(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
       return launch_grouped_mlp_bf16(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
     case MOE_DTYPE_FP8_E4M3_B128:
