@@ -290,10 +290,21 @@ MOE_API moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape
                            const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
                            size_t workspace_bytes, void* out_fc2, void* stream);
 
+/* Number of kernels one moe_grouped_mlp call with these arguments launches
+ * (host only, no device access): 1 where FC1 and FC2 run in one persistent
+ * kernel (bf16 on single SMs), 2 where they are separate launches, 0 for a
+ * zero capacity.  The bf16 path also issues one small memset of its
+ * workspace counters.  Errors: MOE_ERR_INVALID_ARG for a bad shape, layout or
+ * dtype. */
+MOE_API moe_status moe_grouped_mlp_kernel_count(const moe_shape* shape, const moe_layout* layout, int32_t w_dtype,
+                                                int32_t* count_out);
+
 /* Profiling hook: the next moe_grouped_mlp call made by this host thread
  * records the three given CUDA events (cudaEvent_t passed as void*) on its
  * stream -- before FC1, between FC1 and FC2, and after FC2 -- and then forgets
- * them.  Pass NULLs to cancel.  Used to time the two GEMM kernels separately
+ * them.  Where one kernel runs both GEMMs (moe_grouped_mlp_kernel_count 1),
+ * the between and after events are both recorded after it.  Pass NULLs to
+ * cancel.  Used to time the two GEMM kernels separately
  * inside a step (TensorRT-LLM PR #16190 "Update CuTeDSL MegaMoE kernels",
  * commit list: the microbench reports kernel-level times). */
 MOE_API moe_status moe_profile_next_grouped_mlp(void* ev_before_fc1, void* ev_after_fc1, void* ev_after_fc2);

@@ -92,6 +92,8 @@ _SIGNATURES = {
     "moe_grouped_mlp": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                         ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Nvfp4Globals), _P,
                         ctypes.c_size_t, _P, _P],
+    "moe_grouped_mlp_kernel_count": [ctypes.POINTER(_Shape), ctypes.POINTER(_Layout), ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.c_int32)],
     "moe_profile_next_grouped_mlp": [_P, _P, _P],
     "moe_debug_preprocess_silent_tile": [ctypes.POINTER(_Routing), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                                          ctypes.POINTER(_HandleDev), _P, ctypes.c_size_t, ctypes.c_int64, _P],
@@ -247,6 +249,13 @@ def moe_grouped_mlp_workspace_size(shape: Shape, layout: Layout, w_dtype: int) -
     out = ctypes.c_size_t()
     _check(_lib.moe_grouped_mlp_workspace_size(ctypes.byref(shape.c()), ctypes.byref(layout.c()), w_dtype,
                                                ctypes.byref(out)), "moe_grouped_mlp_workspace_size")
+    return out.value
+
+
+def moe_grouped_mlp_kernel_count(shape: Shape, layout: Layout, w_dtype: int) -> int:
+    out = ctypes.c_int32()
+    _check(_lib.moe_grouped_mlp_kernel_count(ctypes.byref(shape.c()), ctypes.byref(layout.c()), w_dtype,
+                                             ctypes.byref(out)), "moe_grouped_mlp_kernel_count")
     return out.value
 
 

@@ -6,7 +6,8 @@ namespace moe {
 
 cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                     const void* perm_tokens, const void* w13, const void* w2, void* act,
-                                    void* out_fc2, cudaStream_t st);
+                                    void* ready, void* out_fc2, cudaStream_t st);
+size_t grouped_mlp_bf16_ready_bytes(const moe_shape& s, const moe_layout& l);
 
 cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                          const void* perm_tokens, const void* w13, const void* w2, void* act,
@@ -30,14 +31,32 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 size_t grouped_mlp_workspace_bytes(const moe_shape& s, const moe_layout& l, int32_t w_dtype) {
   const size_t cap = (size_t)l.capacity, I = (size_t)s.I;
   switch (w_dtype) {
-    case MOE_DTYPE_BF16:
-      return round_up(cap * I * 2, 1024) + 1024;
+    case MOE_DTYPE_BF16:  // bf16 intermediate + FC1 completion counters per M tile
+      return round_up(cap * I * 2, 1024) + round_up(grouped_mlp_bf16_ready_bytes(s, l), 1024) + 1024;
     case MOE_DTYPE_FP8_E4M3_B128:  // E4M3 intermediate + fp32 scales per 128 elements
       return round_up(cap * I, 1024) + round_up(cap * (I / 128) * 4, 1024) + 1024;
     case MOE_DTYPE_NVFP4:  // packed E2M1 intermediate + E4M3 scales per 16 elements
       return round_up(cap * I / 2, 1024) + round_up(cap * (I / 16), 1024) + 1024;
   }
   return 0;
+}
+
+bool grouped_mlp_bf16_uses_pairs(const moe_shape& s, const moe_layout& l) {
+  // Experts with thousands of rows run each MMA across an SM pair (256-row
+  // tiles); otherwise 128-row tiles on single SMs waste fewer rows on the
+  // ragged last tile of each expert segment.
+  return l.capacity >= kPairMinRowsPerExpert * s.E;
+}
+
+int grouped_mlp_kernel_count(const moe_shape& s, const moe_layout& l, int32_t w_dtype) {
+  switch (w_dtype) {
+    case MOE_DTYPE_BF16:  // one fused FC1 + FC2 kernel on single SMs; two kernels on SM pairs
+      return l.capacity == 0 ? 0 : grouped_mlp_bf16_uses_pairs(s, l) ? 2 : 1;
+    case MOE_DTYPE_FP8_E4M3_B128:
+    case MOE_DTYPE_NVFP4:
+      return l.capacity == 0 ? 0 : 2;
+  }
+  return -1;
 }
 
 cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
@@ -47,12 +66,11 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                void* workspace, void* out_fc2, cudaStream_t st) {
   switch (w_dtype) {
     case MOE_DTYPE_BF16:
-      // Experts with thousands of rows run each MMA across an SM pair (256-row
-      // tiles); otherwise 128-row tiles on single SMs waste fewer rows on the
-      // ragged last tile of each expert segment.
-      if (l.capacity >= kPairMinRowsPerExpert * s.E)
+      if (grouped_mlp_bf16_uses_pairs(s, l))
         return launch_grouped_mlp_bf16_pair(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
-      return launch_grouped_mlp_bf16(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
+      return launch_grouped_mlp_bf16(h, s, l, perm_tokens, w13, w2, workspace,
+                                     static_cast<uint8_t*>(workspace) + round_up((size_t)l.capacity * s.I * 2, 1024),
+                                     out_fc2, st);
     case MOE_DTYPE_FP8_E4M3_B128:
       return launch_grouped_mlp_fp8(h, s, l, perm_tokens, perm_scales, w13, w13_scales, w2, w2_scales, workspace,
                                     out_fc2, st);

@@ -211,6 +211,17 @@ moe_status moe_grouped_mlp_workspace_size(const moe_shape* shape, const moe_layo
   return MOE_OK;
 }
 
+moe_status moe_grouped_mlp_kernel_count(const moe_shape* shape, const moe_layout* layout, int32_t w_dtype,
+                                        int32_t* count_out) {
+  MOE_TRY(check_shape(shape, true));
+  MOE_TRY(check_layout(layout));
+  if (!count_out || shape->I <= 0 || shape->I % 128 != 0) return MOE_ERR_INVALID_ARG;
+  const int n = grouped_mlp_kernel_count(*shape, *layout, w_dtype);
+  if (n < 0) return MOE_ERR_INVALID_ARG;
+  *count_out = n;
+  return MOE_OK;
+}
+
 moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
                            int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
                            const void* w13, const void* w13_scales, const void* w2,

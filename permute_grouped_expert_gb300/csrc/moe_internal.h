@@ -59,6 +59,7 @@ cudaError_t launch_quantize_nvfp4_rows(const void* x, int64_t R, int64_t Kd, con
 
 // Grouped MLP (bf16 / FP8 / NVFP4), defined in the GEMM translation units.
 size_t grouped_mlp_workspace_bytes(const moe_shape& s, const moe_layout& l, int32_t w_dtype);
+int grouped_mlp_kernel_count(const moe_shape& s, const moe_layout& l, int32_t w_dtype);
 cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
                                const void* w13, const void* w13_scales, const void* w2,
