@@ -6,17 +6,21 @@
 // caller buffer) and TensorRT-LLM PR #16190 "Update CuTeDSL MegaMoE kernels"
 // (w3_w1 FC1 weight; a persistent tile scheduler over experts).
 //
-// One persistent launch runs both GEMMs: every CTA walks its share of the FC1
-// tiles, then of the FC2 tiles.  An FC2 tile reads the SwiGLU intermediate
-// rows of one M tile, so its producer first waits (bounded) on that M tile's
-// completion counter, which each FC1 epilogue warp raises with a release add
-// after its rows are stored; no kernel boundary separates the two GEMMs, and
-// the tail of FC1 overlaps the start of FC2.
+// One persistent launch runs both GEMMs.  The tile list holds every FC1 tile,
+// then every FC2 tile; CTAs claim tiles in that order from a global counter
+// (one tile ahead), so fast CTAs take more tiles and all finish together.  An
+// FC2 tile reads the SwiGLU intermediate rows of one M tile, so its producer
+// first waits (bounded) on that M tile's completion counter, which each FC1
+// epilogue warp raises with a release add after its rows are stored; no kernel
+// boundary separates the two GEMMs, and the tail of FC1 overlaps the start of
+// FC2.
 //
 // One CTA per SM, warp-specialised:
-//   warp 0      TMA producer: A tile 128 rows x 64 K of the expert's rows, B tile
-//               256 rows x 64 K of its weights (two 128-row boxes), 128-byte
-//               swizzle, 4-stage shared-memory ring (48 KB per stage).
+//   warp 0      claims tiles and passes their ids to the other roles through a
+//               4-slot shared-memory queue; TMA producer: A tile 128 rows x
+//               64 K of the expert's rows, B tile 256 rows x 64 K of its
+//               weights (two 128-row boxes), 128-byte swizzle, 4-stage
+//               shared-memory ring (48 KB per stage).
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
 //               issues tcgen05.mma (M=128, N=256, K=16) from one thread;
 //               tcgen05.commit frees ring stages and publishes accumulators.
@@ -42,6 +46,7 @@ constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
+constexpr int kQueue = 4;  // claimed tile ids in flight from the producer to the MMA and epilogue warps
 constexpr uint32_t kTileABytes = BM * BK * 2;
 constexpr uint32_t kTileBBytes = BN * BK * 2;
 constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;
@@ -63,6 +68,7 @@ struct PhaseParams {
 struct FusedParams {
   const int32_t* offsets;  // [E+1] padded segment offsets
   int32_t* status;         // device status word (timeouts)
+  int32_t* sched;          // tile claim counter, zeroed before the launch
   int32_t* ready;          // [M tiles] FC1 completions per M tile, zeroed before the launch
   PhaseParams ph[2];
   int E, cap;
@@ -142,6 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             FusedParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_tfull[2], s_tempty[2], s_drain;
+  __shared__ __align__(8) uint64_t s_qfull[kQueue], s_qempty[kQueue];
+  __shared__ int s_tile[kQueue];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_prefix[kMaxE + 1];
@@ -160,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; a++) {
       mbar_init(&s_tfull[a], 1);
       mbar_init(&s_tempty[a], kEpiWarps);
+    }
+    for (int q = 0; q < kQueue; q++) {
+      mbar_init(&s_qfull[q], 1);
+      mbar_init(&s_qempty[q], 1 + kEpiWarps);
     }
     mbar_init(&s_drain, 1);
     fence_barrier_init();
@@ -217,7 +229,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; s++) issued[s] = false;
       bool ok = true;
       int ready_g = -1;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int q = 0;
+      uint32_t qphase = 0;
+      int t = atomicAdd(p.sched, 1);
+      for (;;) {
+        // hand the claimed tile (or the end mark) to the MMA and epilogue warps
+        if (!mbar_wait(&s_qempty[q], qphase ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        s_tile[q] = t < total ? t : -1;
+        mbar_arrive(&s_qfull[q]);
+        if (++q == kQueue) {
+          q = 0;
+          qphase ^= 1;
+        }
+        if (t >= total) break;
+        // claim the next tile now, so the claim's round trip overlaps this tile's loads
+        const int next = atomicAdd(p.sched, 1);
         const TileInfo ti = decode_tile(t, total1, s_prefix, p);
         const bool fc2 = ti.phase != 0;
         if (fc2 && ti.g != ready_g) {
@@ -252,6 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1;
           }
         }
+        if (!ok) break;
+        t = next;
       }
       if (!ok) {
         // drain: every copy issued into this CTA's shared memory must land before exit
@@ -270,7 +301,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int q = 0;
+      uint32_t qphase = 0;
+      for (;;) {
+        if (!mbar_wait(&s_qfull[q], qphase, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const int t = s_tile[q];
+        mbar_arrive(&s_qempty[q]);
+        if (++q == kQueue) {
+          q = 0;
+          qphase ^= 1;
+        }
+        if (t < 0) break;
         const int nkb = t >= total1 ? p.ph[1].nkb : p.ph[0].nkb;
         if (!mbar_wait(&s_tempty[acc], acc_phase ^ 1, abort_flag, p.status)) {
           ok = false;
@@ -316,11 +360,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane_base = 32 * (warp & 3);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile(t, total1, s_prefix, p);
+    int q = 0;
+    uint32_t qphase = 0;
+    for (;;) {
       // one lane waits and the warp follows its verdict, so the warp-wide
       // tcgen05.ld below is always executed by all 32 lanes or by none
-      int ok = 0;
+      int ok = 0, t = -1;
+      if (lane == 0 && mbar_wait(&s_qfull[q], qphase, abort_flag, p.status)) {
+        ok = 1;
+        t = s_tile[q];
+        mbar_arrive(&s_qempty[q]);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (++q == kQueue) {
+        q = 0;
+        qphase ^= 1;
+      }
+      if (!ok || t < 0) break;
+      const TileInfo ti = decode_tile(t, total1, s_prefix, p);
       if (lane == 0) ok = mbar_wait(&s_tfull[acc], acc_phase, abort_flag, p.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
@@ -376,14 +434,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+// Synchronisation words in the workspace: the tile claim counter, padded to
+// 128 bytes, then one FC1 completion counter per M tile.
+constexpr size_t kSchedBytes = 128;
 size_t grouped_mlp_bf16_ready_bytes(const moe_shape& s, const moe_layout& l) {
-  return (size_t)((l.capacity + BM - 1) / BM + s.E + 1) * sizeof(int32_t);
+  return kSchedBytes + (size_t)((l.capacity + BM - 1) / BM + s.E + 1) * sizeof(int32_t);
 }
 
 // FC1 and FC2 in one persistent launch.  An FC2 tile waits (bounded) for the
-// FC1 tiles of its M tile, which come earlier in every CTA's tile sequence;
-// with one CTA per SM and the grid no larger than the SM count all CTAs are
-// resident together, so every wait is on work that is running or done.
+// FC1 tiles of its M tile.  Tiles are claimed in list order and every FC1 tile
+// precedes every FC2 tile, so those FC1 tiles were claimed earlier by CTAs
+// that hold no FC2 tile in front of them (a CTA's tile claimed after an FC2
+// tile is an FC2 tile); with one CTA per SM and the grid no larger than the SM
+// count all CTAs are resident together, so every wait is on work that is
+// running or done.
 cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                     const void* perm_tokens, const void* w13, const void* w2, void* act,
                                     void* ready, void* out_fc2, cudaStream_t st) {
@@ -415,7 +479,8 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
   FusedParams p;
   p.offsets = h.padded_offsets;
   p.status = h.status;
-  p.ready = static_cast<int32_t*>(ready);
+  p.sched = static_cast<int32_t*>(ready);
+  p.ready = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ready) + kSchedBytes);
   p.E = (int)s.E;
   p.cap = (int)l.capacity;
   PhaseParams& p1 = p.ph[0];
