@@ -49,6 +49,27 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def profiled_traffic(workload: str, kernel_source: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
+    kernel, from an ncu summary under profiles/ -- only while the kernel's source
+    file still has the hash recorded with the counters, else None."""
+    import glob
+    import hashlib
+    src = os.path.join(ROOT, kernel_source)
+    if not os.path.exists(src):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(path).read()
+        for block in text.split("```roofline-traffic")[1:]:
+            fields = dict(line.split(":", 1) for line in block.split("```")[0].strip().splitlines() if ":" in line)
+            fields = {k.strip(): v.strip() for k, v in fields.items()}
+            if (fields.get("kernel_source") == kernel_source and fields.get("source_sha256") == digest
+                    and fields.get("workload") == workload):
+                return int(fields["traffic_bytes_per_launch"])
+    return None
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -363,6 +384,7 @@ def run_ours(args, w):
             achieved = flops / (t_fc1 * 1e-3) / 1e12
             breakdown.update({"fused_mlp_kernel_ms": round(t_fc1, 5), "fused_mlp_tflops": round(achieved, 1)})
             kernel = "grouped_mlp_bf16 (FC1 + SwiGLU + FC2, one kernel)"
+            traffic = profiled_traffic(w.name, "permute_grouped_expert_gb300/csrc/gemm_bf16.cu")
         else:
             achieved = prob.fc1_flops(R) / (t_fc1 * 1e-3) / 1e12
             breakdown.update({"fc1_ms": round(t_fc1, 5), "fc2_ms": round(t_fc2, 5),
@@ -370,8 +392,9 @@ def run_ours(args, w):
                               "fc2_tflops": round(prob.fc2_flops(R) / (t_fc2 * 1e-3) / 1e12, 1),
                               "fc2_frac_of_peak": round(prob.fc2_flops(R) / (t_fc2 * 1e-3) / 1e12 / peak, 4)})
             kernel = "grouped_fc1_swiglu"
+            traffic = None
         roof = {"kernel": kernel, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_source}
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_source}
     breakdown["dispatch_frac_of_hbm"] = round(breakdown["dispatch_gbs"] / peaks["hbm_gbs"], 4)
     breakdown["combine_frac_of_hbm"] = round(breakdown["combine_gbs"] / peaks["hbm_gbs"], 4)
 
