@@ -21,7 +21,10 @@
 //   warp 1      TMEM allocation (512 columns = 2 partials of 128 x 256 fp32) and
 //               MMA issue from one thread
 //   warps 2..9  two groups of four: group h holds TMEM columns [128h, 128h+128)
-//               of every row, one row per thread; 128 fp32 accumulators each.
+//               of every row, one row per thread; 128 fp32 accumulators each,
+//               folded in with packed fp32x2 FMAs from 16-column TMEM loads
+//               (the 10-warp CTA is budgeted 168 registers a thread; wider loads
+//               spill accumulators to local memory inside the K loop).
 // FC1's weight tile interleaves up and gate rows in 64-row boxes so that each
 // thread ends a tile holding the up and gate values of the same 64 output
 // columns.  Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit).
@@ -62,6 +65,22 @@ MOE_DEVICE void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes, load and wait in one statement.
+MOE_DEVICE void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
 struct Fp8Params {
@@ -291,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bs0 = p.b_scales + ((int64_t)ti.e * p.n_blocks_b + blk_c) * nsb;
         bs1 = bs0;
       }
-      float acc[128];
+      float2 acc2[64];
 #pragma unroll
-      for (int j = 0; j < 128; j++) acc[j] = 0.0f;
+      for (int j = 0; j < 64; j++) acc2[j] = make_float2(0.0f, 0.0f);
       // scales of the next K block are loaded while this one is folded in
       float sa_next = row_in ? __ldg(arow) : 0.0f;
       float sb0_next = __ldg(bs0), sb1_next = __ldg(bs1);
@@ -315,12 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(buf * BN + grp * 128);
         const float s0 = sa * sb0, s1 = sa * sb1;
 #pragma unroll
-        for (int c = 0; c < 4; c++) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const float s = (kMode == kFc1SwiGLU) ? (c < 2 ? s0 : s1) : s0;
+        for (int c = 0; c < 8; c++) {
+          float v[16];
+          tmem_ld16(taddr + c * 16, v);
+          const float s = (kMode == kFc1SwiGLU) ? (c < 4 ? s0 : s1) : s0;
+          const float2 s2 = make_float2(s, s);
 #pragma unroll
-          for (int j = 0; j < 32; j++) acc[c * 32 + j] = fmaf(s, v[j], acc[c * 32 + j]);
+          for (int j = 0; j < 8; j++)
+            acc2[c * 8 + j] = __ffma2_rn(s2, make_float2(v[2 * j], v[2 * j + 1]), acc2[c * 8 + j]);
         }
         tc_fence_before();
         __syncwarp();
@@ -332,13 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       const bool valid = row < ti.row_end;
+      float* acc = reinterpret_cast<float*>(acc2);
       if (kMode == kFc1SwiGLU) {
         // acc[0..63] = up, acc[64..127] = gate of output columns n*128 + 64*grp + j
         float amax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 64; j++) {
           const float g = acc[64 + j];
-          const float a = g / (1.0f + __expf(-g)) * acc[j];
+          const float a = __fdividef(g, 1.0f + __expf(-g)) * acc[j];
           acc[j] = a;
           amax = fmaxf(amax, fabsf(a));
         }
