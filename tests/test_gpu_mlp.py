@@ -147,3 +147,67 @@ def test_overflowed_capacity_layer(oracle, moe):
     yref = oracle.combine(o_full, pre["row_of"], po)
     o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"], po)
     assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(yref), o_rows, wts) <= TOL_BF16
+
+
+def test_whole_layer_in_one_cuda_graph(oracle, moe):
+    """preprocess -> dispatch -> fused grouped MLP -> combine captured once and
+    replayed with new routing and activations written into the same input
+    buffers: the MLP's claim and completion counters are re-zeroed inside the
+    graph, and every replay matches the oracle's per-token layer."""
+    w = _case("tiny", T=384, H=512, E=8, K=2, I=256)
+    cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
+    fmt, rmap, probs = workloads.routing_inputs(w, seed=0)
+    shape, layout = moe.Shape(w.T, w.H, w.E, w.K, w.I), moe.Layout(w.m, cap)
+    assert moe.moe_grouped_mlp_kernel_count(shape, layout, moe.DTYPE_BF16) == 1
+    map_d, probs_d = torch.from_numpy(rmap).cuda(), torch.from_numpy(probs).cuda()
+    x_d = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    w13, w2 = workloads.expert_weights(w, 0, device="cuda")
+    routing = moe.Routing(fmt, map_d, probs_d)
+    handle = moe.Handle.empty(shape, layout)
+    ws = torch.empty(moe.moe_preprocess_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    mlp_ws = torch.empty(moe.moe_grouped_mlp_workspace_size(shape, layout, moe.DTYPE_BF16), dtype=torch.uint8,
+                         device="cuda")
+    y = torch.zeros(cap, w.H, dtype=torch.bfloat16, device="cuda")
+    yp = torch.zeros(cap, dtype=torch.float32, device="cuda")
+    o = torch.zeros(cap, w.H, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+
+    def layer(s):
+        moe.moe_preprocess(routing, shape, layout, handle, ws, stream=s)
+        moe.moe_dispatch_permute(handle, shape, layout, moe.DTYPE_BF16, x_d, None, routing, y, yp, stream=s)
+        moe.moe_grouped_mlp(handle, shape, layout, moe.DTYPE_BF16, y, None, w13, None, w2, None, None, mlp_ws, o,
+                            stream=s)
+        moe.moe_combine_unpermute(handle, shape, layout, o, yp, out, stream=s)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        x_d.copy_(workloads.activations(w, 0).cuda())
+        layer(s)  # eager warm-up (one-time attribute set-up happens outside the capture)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            layer(s)
+    torch.cuda.synchronize()
+    w13b, w2b = workloads.bf16_bits(w13), workloads.bf16_bits(w2)
+    for cycle in range(3):
+        fmt, rmap, probs = workloads.routing_inputs(w, seed=200 + cycle)
+        x = workloads.activations(w, 200 + cycle)
+        map_d.copy_(torch.from_numpy(rmap))
+        probs_d.copy_(torch.from_numpy(probs))
+        x_d.copy_(x.cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(handle.status.item()) == 0
+        pre = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, cap)
+        v = pre["valid_rows"]
+        yo, po = oracle.dispatch(fmt, rmap, probs, pre, workloads.bf16_bits(x), cap, w.E, w.K)
+        ob, _ = oracle.grouped_mlp_rows(0, yo, None, w.H, w.I, w.E, pre["offsets"], w13b, None, w2b, None,
+                                        np.arange(v))
+        assert rel_err(oracle.bf16_to_f64(bits(o)[:v]), oracle.bf16_to_f64(ob)) <= TOL_BF16
+        ref = oracle.layer_per_token(0, fmt, rmap, probs, w.E, w.K, workloads.bf16_bits(x), None, w.H, w.I, w13b,
+                                     None, w2b, None, np.arange(w.T))
+        o_full = np.zeros((cap, w.H), np.uint16)
+        o_full[:v] = ob
+        o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"], po)
+        assert layer_rel_err(oracle.bf16_to_f64(bits(out)), oracle.bf16_to_f64(ref), o_rows, wts) <= TOL_BF16
