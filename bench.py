@@ -260,6 +260,32 @@ class Problem:
     def fc2_flops(self, R):
         return 2.0 * R * self.w.I * self.w.H
 
+    def active_experts(self) -> int:
+        import torch
+        torch.cuda.synchronize()
+        return int(self.handle.tokens_per_expert.gt(0).sum().item())
+
+    def _elem_bytes(self, n):
+        """Bytes of n values stored as bf16, or as NVFP4 (packed E2M1 + one E4M3 scale per 16)."""
+        return n / 2 + n / 16 if self.w.dtype == "nvfp4" else 2.0 * n
+
+    def fc1_bytes(self, R, active):
+        """FC1 algorithmic bytes: the active experts' w3_w1, the dispatched rows, the intermediate written."""
+        w = self.w
+        if w.dtype == "fp8":
+            wb = 2 * w.I * w.H + 4 * (2 * w.I // 128) * (w.H // 128)
+            return active * wb + R * (w.H + 4 * w.H // 128) + R * (w.I + 4 * w.I // 128)
+        wb = self._elem_bytes(2 * w.I * w.H)
+        return active * wb + R * self._elem_bytes(w.H) + R * self._elem_bytes(w.I)
+
+    def fc2_bytes(self, R, active):
+        """FC2 algorithmic bytes: the active experts' w2, the intermediate read, the bf16 output written."""
+        w = self.w
+        if w.dtype == "fp8":
+            wb = w.H * w.I + 4 * (w.H // 128) * (w.I // 128)
+            return active * wb + R * (w.I + 4 * w.I // 128) + R * 2 * w.H
+        return active * self._elem_bytes(w.H * w.I) + R * self._elem_bytes(w.I) + R * 2 * w.H
+
     def dispatch_bytes(self, R):
         w = self.w
         row_in = {"bf16": 2 * w.H, "fp8": 2 * w.H, "nvfp4": 2 * w.H}[w.dtype]
@@ -385,16 +411,37 @@ def run_ours(args, w):
             breakdown.update({"fused_mlp_kernel_ms": round(t_fc1, 5), "fused_mlp_tflops": round(achieved, 1)})
             kernel = "grouped_mlp_bf16 (FC1 + SwiGLU + FC2, one kernel)"
             traffic = profiled_traffic(w.name, "permute_grouped_expert_gb300/csrc/gemm_bf16.cu")
+        elif w.dtype == "nvfp4":
+            # decode: a few rows per expert, so FC1 streams the active experts' weights (HBM-bound)
+            active = prob.active_experts()
+            fc1_bytes = prob.fc1_bytes(R, active)
+            achieved_gbs = fc1_bytes / (t_fc1 * 1e-3) / 1e9
+            breakdown.update({"fc1_ms": round(t_fc1, 5), "fc2_ms": round(t_fc2, 5), "active_experts": active,
+                              "fc1_tflops": round(prob.fc1_flops(R) / (t_fc1 * 1e-3) / 1e12, 2),
+                              "fc1_weight_gbs": round(achieved_gbs, 1),
+                              "fc2_weight_gbs": round(prob.fc2_bytes(R, active) / (t_fc2 * 1e-3) / 1e9, 1)})
+            roof = {"kernel": "grouped_fc1_swiglu (NVFP4)", "bound": "hbm", "achieved": round(achieved_gbs, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
+                    "traffic": None, "peak_source": f"{peak_src} hbm_gbs"}
+            kernel = None
         else:
             achieved = prob.fc1_flops(R) / (t_fc1 * 1e-3) / 1e12
+            if w.dtype == "fp8":
+                active = prob.active_experts()
+                breakdown["fc1_weight_hbm_frac"] = round(
+                    prob.fc1_bytes(R, active) / (t_fc1 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+                breakdown["fc2_weight_hbm_frac"] = round(
+                    prob.fc2_bytes(R, active) / (t_fc2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
             breakdown.update({"fc1_ms": round(t_fc1, 5), "fc2_ms": round(t_fc2, 5),
                               "fc1_tflops": round(achieved, 1),
                               "fc2_tflops": round(prob.fc2_flops(R) / (t_fc2 * 1e-3) / 1e12, 1),
                               "fc2_frac_of_peak": round(prob.fc2_flops(R) / (t_fc2 * 1e-3) / 1e12 / peak, 4)})
             kernel = "grouped_fc1_swiglu"
             traffic = None
-        roof = {"kernel": kernel, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_source}
+        if kernel is not None:
+            roof = {"kernel": kernel, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "peak_source": peak_source}
     breakdown["dispatch_frac_of_hbm"] = round(breakdown["dispatch_gbs"] / peaks["hbm_gbs"], 4)
     breakdown["combine_frac_of_hbm"] = round(breakdown["combine_gbs"] / peaks["hbm_gbs"], 4)
 
@@ -419,7 +466,8 @@ def run_ours(args, w):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.seed, sample_tokens=args.cpu_sample_tokens)
+        line["cpu_baseline"] = cpu_baseline(w, args.seed, sample_tokens=args.cpu_sample_tokens,
+                                            target_s=args.cpu_seconds)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -429,62 +477,100 @@ def run_ours(args, w):
 
 # ----------------------------------------------------------- CPU oracle arm
 
-def cpu_baseline(w, seed, sample_tokens=16):
+def _nvfp4_global(a) -> float:
+    """fp32 global scale amax / (6 * 448) of a tensor (the value the GPU side computes on the host too)."""
+    return float(np.float32(float(np.abs(np.asarray(a, np.float32)).max()) / 2688.0))
+
+
+def cpu_baseline(w, seed, sample_tokens=16, target_s=None):
     """The oracle as it stands, on a bounded sample: full preprocess and dispatch
-    (they scale with T), the MLP and combine for `sample_tokens` tokens (all
-    their routes), extrapolated to the whole batch.  Returns tokens/s."""
+    (they scale with T), then the MLP and combine for sampled tokens (all their
+    routes), extrapolated to the whole batch.  Without target_s the sample is
+    `sample_tokens` tokens; with it, batches of new tokens (starting at one and
+    growing with the measured rate) are added until the sampled part has taken
+    target_s seconds or every token is in.  Returns the cpu_baseline object."""
     import oracle
     import torch
 
     oracle.build()
     cores = os.cpu_count()
     fmt, rmap, probs = workloads.routing_inputs(w, seed)
-    x = workloads.bf16_bits(workloads.activations(w, seed))
+    x_t = workloads.activations(w, seed)
+    x = workloads.bf16_bits(x_t)
     t0 = time.perf_counter()
     cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
     if w.cap_factor:
         cap = oracle.capacity(oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, cap)["total_rows"], w.cap_factor)
     pre = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, cap)
+    ys = None
+    gx = 0.0
     if w.dtype == "fp8":
         xq, xs = oracle.quantize_fp8_rows(x)
         yq, yp = oracle.dispatch(fmt, rmap, probs, pre, xq, cap, w.E, w.K)
         ys, _ = oracle.dispatch(fmt, rmap, None, pre, xs, cap, w.E, w.K)
+    elif w.dtype == "nvfp4":
+        gx = _nvfp4_global(x_t.float().numpy())
+        xq, xs = oracle.quantize_nvfp4_rows(x, gx)
+        yq, yp = oracle.dispatch(fmt, rmap, probs, pre, xq, cap, w.E, w.K)
+        ys, _ = oracle.dispatch(fmt, rmap, None, pre, xs, cap, w.E, w.K)
     else:
         yq, yp = oracle.dispatch(fmt, rmap, probs, pre, x, cap, w.E, w.K)
-        ys = None
     t_full = time.perf_counter() - t0
-    n = min(sample_tokens, w.T)
-    toks = np.random.default_rng(0).choice(w.T, n, replace=False)
-    t1 = time.perf_counter()
-    if w.I:
-        rows = pre["row_of"][toks]
-        rows = np.unique(rows[rows >= 0])
-        experts = sorted({int(np.searchsorted(pre["offsets"], r, side="right") - 1) for r in rows})
-        w13, w2 = workloads.expert_weights(w, seed, experts=experts)
-        fmt_mlp = 0
-        w13b, w2b, s13, s2 = workloads.bf16_bits(w13), workloads.bf16_bits(w2), None, None
-        if w.dtype == "fp8":
-            fmt_mlp = 1
-            w13b, s13 = oracle.quantize_fp8_weight(w13b)
-            w2b, s2 = oracle.quantize_fp8_weight(w2b)
-        sel, off = [], [0]
-        for e in experts:
-            rr = rows[(rows >= pre["offsets"][e]) & (rows < pre["offsets"][e + 1])]
-            sel.append(rr)
-            off.append(off[-1] + len(rr))
-        sel = np.concatenate(sel)
-        ob, _ = oracle.grouped_mlp_rows(fmt_mlp, yq[sel], None if ys is None else ys[sel], w.H, w.I, len(experts),
-                                        np.array(off, np.int32), w13b, s13, w2b, s2, np.arange(len(sel)))
-        o_full = np.zeros((cap, w.H), np.uint16)
-        o_full[sel] = ob
-    else:
-        o_full = yq
-    oracle.combine(o_full, pre["row_of"][toks], yp)
-    t_sample = time.perf_counter() - t1
-    est = t_full + t_sample * (w.T / n)
+
+    order = np.random.default_rng(0).permutation(w.T)
+    done, t_sample = 0, 0.0
+    n = 1 if target_s is not None else sample_tokens
+    while done < w.T:
+        n = min(n, w.T - done)
+        toks = order[done:done + n]
+        t1 = time.perf_counter()
+        if w.I:
+            rows = pre["row_of"][toks]
+            rows = np.unique(rows[rows >= 0])
+            experts = sorted({int(np.searchsorted(pre["offsets"], r, side="right") - 1) for r in rows})
+            w13, w2 = workloads.expert_weights(w, seed, experts=experts)
+            w13b, w2b = workloads.bf16_bits(w13), workloads.bf16_bits(w2)
+            s13 = s2 = None
+            extra = {}
+            fmt_mlp = 0
+            if w.dtype == "fp8":
+                fmt_mlp = 1
+                w13b, s13 = oracle.quantize_fp8_weight(w13b)
+                w2b, s2 = oracle.quantize_fp8_weight(w2b)
+            elif w.dtype == "nvfp4":
+                fmt_mlp = 2
+                g13 = np.array([_nvfp4_global(w13[j].float().numpy()) for j in range(len(experts))], np.float32)
+                g2 = np.array([_nvfp4_global(w2[j].float().numpy()) for j in range(len(experts))], np.float32)
+                q13 = [oracle.quantize_nvfp4_rows(w13b[j], float(g13[j])) for j in range(len(experts))]
+                q2 = [oracle.quantize_nvfp4_rows(w2b[j], float(g2[j])) for j in range(len(experts))]
+                w13b, s13 = np.stack([a for a, _ in q13]), np.stack([b for _, b in q13])
+                w2b, s2 = np.stack([a for a, _ in q2]), np.stack([b for _, b in q2])
+                extra = dict(w13_global=g13, w2_global=g2, fc1_in_global=gx, fc2_in_global=float(np.float32(0.01)))
+            sel, off = [], [0]
+            for e in experts:
+                rr = rows[(rows >= pre["offsets"][e]) & (rows < pre["offsets"][e + 1])]
+                sel.append(rr)
+                off.append(off[-1] + len(rr))
+            sel = np.concatenate(sel)
+            ob, _ = oracle.grouped_mlp_rows(fmt_mlp, yq[sel], None if ys is None else ys[sel], w.H, w.I,
+                                            len(experts), np.array(off, np.int32), w13b, s13, w2b, s2,
+                                            np.arange(len(sel)), **extra)
+            o_full = np.zeros((cap, w.H), np.uint16)
+            o_full[sel] = ob
+        else:
+            o_full = yq
+        oracle.combine(o_full, pre["row_of"][toks], yp)
+        t_sample += time.perf_counter() - t1
+        done += n
+        if target_s is None or t_sample >= target_s:
+            break
+        # next batch: what the rate so far says is left to reach target_s, at most doubling
+        per_token = t_sample / done
+        n = max(1, min(2 * done, sample_tokens * 64, int((target_s - t_sample) / max(per_token, 1e-9)) + 1))
+    est = t_full + t_sample * (w.T / done)
     return {"value": round(w.T / est, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"full preprocess + dispatch of {w.T} tokens ({t_full:.2f} s); grouped MLP + combine of "
-                      f"{n} sampled tokens ({t_sample:.2f} s) extrapolated x{w.T / n:.0f}"}
+                      f"{done} sampled tokens ({t_sample:.2f} s) extrapolated x{w.T / done:.1f}"}
 
 
 def run_reference(args, w):
@@ -521,7 +607,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=16, help="batch-size scale of the CPU oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="the CPU oracle baseline samples batches until its MLP + combine part took this long")
     ap.add_argument("--ref-sample-tokens", type=int, default=4)
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=INT",
                     help="shrink the workload for profiling captures, e.g. --set E=32 --set T=1024")
