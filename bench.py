@@ -224,9 +224,15 @@ class Problem:
         torch.cuda.synchronize()
 
     def step(self, stream, ev=None, prof=None):
-        """The four library calls; ev: list of 5 events recorded between calls."""
+        """The four library calls.  ev: events recorded at the call boundaries --
+        a list of 5 (before and after every call), or a dict {index: event} for
+        a subset of the boundaries 0..4; prof: the grouped-MLP profiling hook's
+        three events."""
         moe = self.moe
-        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        if isinstance(ev, dict):
+            rec = lambda i: ev[i].record(stream) if i in ev else None
+        else:
+            rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
         rec(0)
         moe.moe_preprocess(self.routing, self.shape, self.layout, self.handle, self.ws, stream=stream)
         rec(1)
@@ -326,8 +332,13 @@ def run_ours(args, w):
             prob.step(stream)
     torch.cuda.synchronize()
 
-    # ---- device-timed region: inputs resident in HBM
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    # ---- device-timed region: inputs resident in HBM.  Only the dominant
+    # kernel is bracketed by events here (the grouped-MLP hook's events, or the
+    # dispatch call's boundaries for identity experts); the other calls' times
+    # come from a separate, untimed pass below, so their events do not perturb
+    # the step time.
+    devs = [{1: torch.cuda.Event(enable_timing=True), 2: torch.cuda.Event(enable_timing=True)}
+            for _ in range(K)] if prob.identity else None
     pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)] if not prob.identity else None
     if pevs:
         for trio in pevs:  # create the underlying events before handing them to the library
@@ -345,22 +356,31 @@ def run_ours(args, w):
     with torch.cuda.stream(stream):
         t_begin.record(stream)
         for i in range(K):
-            prob.step(stream, evs[i], pevs[i] if pevs else None)
+            prob.step(stream, devs[i] if devs else None, pevs[i] if pevs else None)
         t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     total_ms = max_over_ranks(t_begin.elapsed_time(t_end), dev)
     ms_step = total_ms / K
 
-    def mean_ms(a, b, table):
-        return statistics.mean(table[i][a].elapsed_time(table[i][b]) for i in range(K))
+    def mean_ms(a, b, table, n):
+        return statistics.mean(table[i][a].elapsed_time(table[i][b]) for i in range(n))
 
-    t_pre = mean_ms(0, 1, evs)
-    t_dis = mean_ms(1, 2, evs)
-    t_mlp = mean_ms(2, 3, evs)
-    t_com = mean_ms(3, 4, evs)
-    t_fc1 = mean_ms(0, 1, pevs) if pevs else None
-    t_fc2 = mean_ms(1, 2, pevs) if pevs else None
+    t_fc1 = mean_ms(0, 1, pevs, K) if pevs else None
+    t_fc2 = mean_ms(1, 2, pevs, K) if pevs else None
+    t_dis_timed = mean_ms(1, 2, devs, K) if devs else None
+
+    # ---- per-call breakdown: a separate pass with events at every call boundary
+    KB = min(K, 50)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KB)]
+    with torch.cuda.stream(stream):
+        for i in range(KB):
+            prob.step(stream, evs[i])
+    torch.cuda.synchronize()
+    t_pre = mean_ms(0, 1, evs, KB)
+    t_dis = t_dis_timed if devs else mean_ms(1, 2, evs, KB)
+    t_mlp = mean_ms(2, 3, evs, KB)
+    t_com = mean_ms(3, 4, evs, KB)
 
     # ---- end to end: pinned host inputs in, result out, every step
     e2e_evs = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
