@@ -1,6 +1,7 @@
 // permute.cu -- dispatch_with_permute, combine with unpermute, and the FP8 /
 // NVFP4 quantizers.  All HBM-bound: 128-bit vector loads and stores, one warp
-// per token, grids sized to fill every SM.
+// per (token, row chunk) work item so that even a decode batch of 64 tokens
+// keeps every SM busy, grids sized to fill every SM.
 //
 // Follows Megatron-LM PR #6800 "Reuse caller-owned HybridEP dispatch and expert
 // output buffers" (Summary: dispatch writes permuted tokens into a caller
@@ -37,6 +38,8 @@ struct DispatchParams {
   uint8_t* out_scales;
   int64_t row_bytes;    // bytes of one output row
   int64_t scale_bytes;  // bytes of one output scale row
+  int64_t nchunks;      // work items per token (row chunks)
+  int64_t chunk_steps;  // loop steps of the row per chunk
 };
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -52,15 +55,16 @@ __device__ __forceinline__ void st_vec(void* p, uint4 v) {
                : "memory");
 }
 
-// Destination rows of token t into this warp's shared slots; also writes the
-// dispatched probabilities.  Returns nothing; callers __syncwarp afterwards.
+// Destination rows of token t into this warp's shared slots; with
+// write_probs also writes the dispatched probabilities (once per token: by the
+// warp that copies the token's first chunk).
 __device__ __forceinline__ void load_dests(const DispatchParams& p, const int32_t* soff, int64_t t,
-                                           int32_t* sdest) {
+                                           int32_t* sdest, bool write_probs) {
   const int lane = threadIdx.x & 31;
   for (int k = lane; k < p.K; k += 32) {
     const int32_t d = p.row_of[t * p.K + k];
     sdest[k] = d;
-    if (d >= 0 && p.out_probs && p.probs) {
+    if (write_probs && d >= 0 && p.out_probs && p.probs) {
       float pr;
       if (p.format == MOE_ROUTING_DENSE_I16)
         pr = p.probs[t * p.K + k];
@@ -98,21 +102,23 @@ __global__ void __launch_bounds__(kThreads) dispatch_copy_kernel(DispatchParams 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nvec = p.row_bytes / 16;
   const int64_t nsc = p.scale_bytes / 4;
-  const int64_t items = p.T + p.E;
+  const int64_t nchunks = p.nchunks;
+  const int64_t items = p.T * nchunks + p.E;
   for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
-    if (it >= p.T) {
-      zero_pads(p, soff, (int)(it - p.T));
+    if (it >= p.T * nchunks) {
+      zero_pads(p, soff, (int)(it - p.T * nchunks));
       continue;
     }
-    const int64_t t = it;
-    load_dests(p, soff, t, s_dest[warp]);
+    const int64_t t = it / nchunks, chunk = it - t * nchunks;
+    load_dests(p, soff, t, s_dest[warp], chunk == 0);
     const uint8_t* src = p.x + t * p.row_bytes;
-    for (int64_t base = 0; base < nvec; base += 32 * kUnroll) {
+    const int64_t vend = min64(nvec, (chunk + 1) * p.chunk_steps * 32 * kUnroll);
+    for (int64_t base = chunk * p.chunk_steps * 32 * kUnroll; base < vend; base += 32 * kUnroll) {
       uint4 v[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; u++) {
         const int64_t idx = base + u * 32 + lane;
-        if (idx < nvec) v[u] = ld_stream(src + idx * 16);
+        if (idx < vend) v[u] = ld_stream(src + idx * 16);
       }
       for (int k = 0; k < p.K; k++) {
         const int32_t d = s_dest[warp][k];
@@ -121,11 +127,11 @@ __global__ void __launch_bounds__(kThreads) dispatch_copy_kernel(DispatchParams 
 #pragma unroll
         for (int u = 0; u < kUnroll; u++) {
           const int64_t idx = base + u * 32 + lane;
-          if (idx < nvec) st_vec(dst + idx * 16, v[u]);
+          if (idx < vend) st_vec(dst + idx * 16, v[u]);
         }
       }
     }
-    if (nsc) {
+    if (nsc && chunk == 0) {
       const float* ssrc = p.x_scales + t * nsc;
       for (int64_t b = lane; b < nsc; b += 32) {
         const float sv = ssrc[b];
@@ -148,23 +154,26 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchParams p
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t H = p.H;
-  const int64_t items = p.T + p.E;
+  const int64_t kChunk = p.chunk_steps * 512;  // elements of a row one work item quantizes
+  const int64_t nchunks = p.nchunks;
+  const int64_t items = p.T * nchunks + p.E;
   for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
-    if (it >= p.T) {
-      zero_pads(p, soff, (int)(it - p.T));
+    if (it >= p.T * nchunks) {
+      zero_pads(p, soff, (int)(it - p.T * nchunks));
       continue;
     }
-    const int64_t t = it;
-    load_dests(p, soff, t, s_dest[warp]);
+    const int64_t t = it / nchunks, chunk = it - t * nchunks;
+    load_dests(p, soff, t, s_dest[warp], chunk == 0);
     const uint8_t* src = p.x + t * H * 2;
-    for (int64_t base = 0; base < H; base += 256 * 2) {
+    const int64_t chunk_end = min64(H, (chunk + 1) * kChunk);
+    for (int64_t base = chunk * kChunk; base < chunk_end; base += 256 * 2) {
       uint2 q[2];
       float sc[2];
       bool live[2];
 #pragma unroll
       for (int u = 0; u < 2; u++) {
         const int64_t e0 = base + u * 256 + lane * 8;
-        live[u] = e0 < H;  // H is a multiple of 128, so a 16-lane block is live or dead as a whole
+        live[u] = e0 < chunk_end;  // H and the chunk are multiples of 128: a 16-lane block is live or dead as a whole
         uint4 v = live[u] ? ld_stream(src + e0 * 2) : make_uint4(0, 0, 0, 0);
         float f[8];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -214,18 +223,21 @@ __global__ void __launch_bounds__(kThreads) dispatch_nvfp4_kernel(DispatchParams
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t H = p.H;
   const float g = *p.x_scales;
-  const int64_t items = p.T + p.E;
+  const int64_t kChunk = p.chunk_steps * 256;  // elements of a row one work item quantizes
+  const int64_t nchunks = p.nchunks;
+  const int64_t items = p.T * nchunks + p.E;
   for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
-    if (it >= p.T) {
-      zero_pads(p, soff, (int)(it - p.T));
+    if (it >= p.T * nchunks) {
+      zero_pads(p, soff, (int)(it - p.T * nchunks));
       continue;
     }
-    const int64_t t = it;
-    load_dests(p, soff, t, s_dest[warp]);
+    const int64_t t = it / nchunks, chunk = it - t * nchunks;
+    load_dests(p, soff, t, s_dest[warp], chunk == 0);
     const uint8_t* src = p.x + t * H * 2;
-    for (int64_t base = 0; base < H; base += 256) {
+    const int64_t chunk_end = min64(H, (chunk + 1) * kChunk);
+    for (int64_t base = chunk * kChunk; base < chunk_end; base += 256) {
       const int64_t e0 = base + lane * 8;
-      const bool live = e0 < H;
+      const bool live = e0 < chunk_end;
       uint4 v = live ? ld_stream(src + e0 * 2) : make_uint4(0, 0, 0, 0);
       float f[8];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -261,6 +273,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_nvfp4_kernel(DispatchParams
 
 struct CombineParams {
   int64_t T, H, K;
+  int64_t nchunks, chunk_steps;  // work items per token; 64-vector steps per item
   const int32_t* row_of;
   const uint8_t* o;
   const float* perm_probs;
@@ -273,7 +286,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineParams p) {
   __shared__ float s_w[kWarps][kMaxK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nvec = p.H / 8;
-  for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < p.T; t += (int64_t)gridDim.x * kWarps) {
+  const int64_t nchunks = p.nchunks;
+  const int64_t items = p.T * nchunks;
+  for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
+    const int64_t t = it / nchunks, chunk = it - t * nchunks;
     int nk = 0;
     for (int k0 = 0; k0 < p.K; k0 += 32) {
       const int k = k0 + lane;
@@ -287,7 +303,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineParams p) {
       nk += __popc(keep);
     }
     __syncwarp();
-    for (int64_t base = 0; base < nvec; base += 64) {
+    const int64_t vend = min64(nvec, (chunk + 1) * p.chunk_steps * 64);
+    for (int64_t base = chunk * p.chunk_steps * 64; base < vend; base += 64) {
       float acc[2][8];
 #pragma unroll
       for (int u = 0; u < 2; u++)
@@ -427,6 +444,20 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const uint8_t*
   }
 }
 
+// Work items per token: a row of `steps` loop steps is split into chunks only
+// when the tokens alone would leave SMs idle (fewer than ~16 warps of work per
+// SM, as in decode batches); long runs of work per warp keep more loads in
+// flight, so large batches keep one item per token.
+void row_split(int64_t T, int64_t steps, int64_t* nchunks, int64_t* chunk_steps) {
+  const int64_t want = (int64_t)device_sm_count() * 16;
+  int64_t n = T > 0 ? (want + T - 1) / T : 1;
+  if (n > steps) n = steps;
+  if (n < 1) n = 1;
+  const int64_t cs = steps > 0 ? (steps + n - 1) / n : 1;
+  *chunk_steps = cs;
+  *nchunks = steps > 0 ? (steps + cs - 1) / cs : 1;
+}
+
 unsigned grid_for(int64_t items_warps) {
   const int64_t per_sm = 2048 / kThreads;
   int64_t blocks = (items_warps + kWarps - 1) / kWarps;
@@ -458,29 +489,33 @@ cudaError_t launch_dispatch(const moe_handle_dev& h, const moe_shape& s, const m
   p.out = static_cast<uint8_t*>(out_tokens);
   p.out_probs = out_probs;
   p.out_scales = static_cast<uint8_t*>(out_scales);
-  const unsigned grid = grid_for(s.T + s.E);
   const size_t smem = (size_t)(s.E + 1) * 4;
+  // one warp per (token, row chunk) work item, plus one per expert for its pad rows
   switch (in_dtype) {
     case MOE_DTYPE_BF16:
       p.row_bytes = s.H * 2;
       p.scale_bytes = 0;
       p.out_scales = nullptr;
-      dispatch_copy_kernel<<<grid, kThreads, smem, st>>>(p);
+      row_split(s.T, (p.row_bytes / 16 + 32 * kUnroll - 1) / (32 * kUnroll), &p.nchunks, &p.chunk_steps);
+      dispatch_copy_kernel<<<grid_for(s.T * p.nchunks + s.E), kThreads, smem, st>>>(p);
       break;
     case MOE_DTYPE_FP8_E4M3_B128:
       p.row_bytes = s.H;
       p.scale_bytes = (s.H / 128) * 4;
-      dispatch_copy_kernel<<<grid, kThreads, smem, st>>>(p);
+      row_split(s.T, (p.row_bytes / 16 + 32 * kUnroll - 1) / (32 * kUnroll), &p.nchunks, &p.chunk_steps);
+      dispatch_copy_kernel<<<grid_for(s.T * p.nchunks + s.E), kThreads, smem, st>>>(p);
       break;
     case MOE_DTYPE_BF16_TO_FP8:
       p.row_bytes = s.H;
       p.scale_bytes = (s.H / 128) * 4;
-      dispatch_fp8_kernel<<<grid, kThreads, smem, st>>>(p);
+      row_split(s.T, (s.H + 511) / 512, &p.nchunks, &p.chunk_steps);
+      dispatch_fp8_kernel<<<grid_for(s.T * p.nchunks + s.E), kThreads, smem, st>>>(p);
       break;
     case MOE_DTYPE_BF16_TO_NVFP4:
       p.row_bytes = s.H / 2;
       p.scale_bytes = s.H / 16;
-      dispatch_nvfp4_kernel<<<grid, kThreads, smem, st>>>(p);
+      row_split(s.T, (s.H + 255) / 256, &p.nchunks, &p.chunk_steps);
+      dispatch_nvfp4_kernel<<<grid_for(s.T * p.nchunks + s.E), kThreads, smem, st>>>(p);
       break;
     default:
       return cudaErrorInvalidValue;
@@ -500,7 +535,8 @@ cudaError_t launch_combine(const moe_handle_dev& h, const moe_shape& s, const mo
   p.o = static_cast<const uint8_t*>(expert_out);
   p.perm_probs = perm_probs;
   p.y = static_cast<uint8_t*>(y);
-  combine_kernel<<<grid_for(s.T), kThreads, 0, st>>>(p);
+  row_split(s.T, (s.H / 8 + 63) / 64, &p.nchunks, &p.chunk_steps);
+  combine_kernel<<<grid_for(s.T * p.nchunks), kThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 
