@@ -309,6 +309,18 @@ MOE_API moe_status moe_grouped_mlp_kernel_count(const moe_shape* shape, const mo
  * commit list: the microbench reports kernel-level times). */
 MOE_API moe_status moe_profile_next_grouped_mlp(void* ev_before_fc1, void* ev_after_fc1, void* ev_after_fc2);
 
+/* Testing hook for the failure path of the fused grouped MLP's bounded waits:
+ * the next moe_grouped_mlp call made by this host thread that runs FC1 and FC2
+ * in one kernel (moe_grouped_mlp_kernel_count 1) lets the FC1 tiles of token
+ * tile `token_tile` (tiles of up to 128 rows, numbered over all experts in
+ * order) withhold their completion publication, so the FC2 tiles that read
+ * those rows give up after about 2 s: MOE_DEV_ERR_TIMEOUT is set in
+ * handle->status and the kernel returns; no kernel traps and the context stays
+ * usable.  That call's outputs are not valid.  -1 cancels.  Other paths clear
+ * the setting without using it.  Errors: MOE_ERR_INVALID_ARG for token_tile <
+ * -1.  Not for production use. */
+MOE_API moe_status moe_debug_next_grouped_mlp_silent_token_tile(int64_t token_tile);
+
 /* Testing hook for the failure path of the bounded inter-CTA waits: runs
  * moe_preprocess with tile `silent_tile` (>= 0) withholding its lookback
  * publication, so every later tile's bounded wait runs out (after about 2 s),

@@ -95,6 +95,7 @@ _SIGNATURES = {
     "moe_grouped_mlp_kernel_count": [ctypes.POINTER(_Shape), ctypes.POINTER(_Layout), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_int32)],
     "moe_profile_next_grouped_mlp": [_P, _P, _P],
+    "moe_debug_next_grouped_mlp_silent_token_tile": [_I64],
     "moe_debug_preprocess_silent_tile": [ctypes.POINTER(_Routing), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                                          ctypes.POINTER(_HandleDev), _P, ctypes.c_size_t, ctypes.c_int64, _P],
     "moe_quantize_fp8_blocks": [_P, _I64, _I64, _I64, _P, _P, _P],
@@ -312,6 +313,13 @@ def moe_profile_next_grouped_mlp(ev_before_fc1, ev_after_fc1, ev_after_fc2) -> N
     handles = [ctypes.c_void_p(e.cuda_event) if e is not None else None
                for e in (ev_before_fc1, ev_after_fc1, ev_after_fc2)]
     _check(_lib.moe_profile_next_grouped_mlp(*handles), "moe_profile_next_grouped_mlp")
+
+
+def moe_debug_next_grouped_mlp_silent_token_tile(token_tile: int) -> None:
+    """Testing hook: the next fused bf16 grouped MLP call lets token tile
+    `token_tile`'s FC1 tiles withhold their completion publication (-1 cancels)."""
+    _check(_lib.moe_debug_next_grouped_mlp_silent_token_tile(token_tile),
+           "moe_debug_next_grouped_mlp_silent_token_tile")
 
 
 def moe_debug_preprocess_silent_tile(routing: Routing, shape: Shape, layout: Layout, handle: Handle,

@@ -88,6 +88,7 @@ struct FusedParams {
   PhaseParams ph[2];
   int E, cap;
   int ready_target;  // kEpiWarps * FC1 feature tiles: a token tile's intermediate rows are complete
+  int silent_g;      // testing hook: FC1 tiles of this token tile withhold their publication (-1: none)
 };
 
 struct TileInfo {
@@ -448,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __threadfence();
         __syncwarp();
-        if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.ready + ti.g) : "memory");
+        if (lane == 0 && ti.g != p.silent_g)
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.ready + ti.g) : "memory");
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_tempty[acc]);
@@ -485,7 +487,7 @@ size_t grouped_mlp_bf16_ready_bytes(const moe_shape& s, const moe_layout& l) {
 // is running or done.
 cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                     const void* perm_tokens, const void* w13, const void* w2, void* act,
-                                    void* ready, void* out_fc2, cudaStream_t st) {
+                                    void* ready, void* out_fc2, cudaStream_t st, int64_t silent_token_tile) {
   if (l.capacity == 0) return cudaSuccess;
   if (s.E > kMaxE) return cudaErrorNotSupported;
   const uint64_t cap = (uint64_t)l.capacity;
@@ -537,6 +539,7 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
   p2.nt = (int)((s.H + 2 * BW - 1) / (2 * BW));
   p2.nkb = (int)(s.I / BK);
   p.ready_target = kEpiWarps * p1.nt;
+  p.silent_g = silent_token_tile >= 0 && silent_token_tile < (int64_t)INT32_MAX ? (int)silent_token_tile : -1;
 
   const int64_t t_tiles_bound = (l.capacity + BT - 1) / BT + s.E;
   int64_t grid = device_sm_count();

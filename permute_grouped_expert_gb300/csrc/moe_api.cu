@@ -62,6 +62,16 @@ ProfileEvents take_profile_events() {
 
 void set_profile_events(const ProfileEvents& ev) { g_profile = ev; }
 
+thread_local int64_t g_debug_mlp_silent = -1;
+
+int64_t take_debug_mlp_silent_tile() {
+  const int64_t v = g_debug_mlp_silent;
+  g_debug_mlp_silent = -1;
+  return v;
+}
+
+void set_debug_mlp_silent_tile(int64_t token_tile) { g_debug_mlp_silent = token_tile; }
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -255,6 +265,12 @@ moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape,
                                      static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status moe_debug_next_grouped_mlp_silent_token_tile(int64_t token_tile) {
+  if (token_tile < -1) return MOE_ERR_INVALID_ARG;
+  set_debug_mlp_silent_tile(token_tile);
+  return MOE_OK;
 }
 
 moe_status moe_profile_next_grouped_mlp(void* ev_before_fc1, void* ev_after_fc1, void* ev_after_fc2) {

@@ -77,6 +77,10 @@ struct ProfileEvents {
   cudaEvent_t before_fc1 = nullptr, after_fc1 = nullptr, after_fc2 = nullptr;
 };
 ProfileEvents take_profile_events();
+// Testing hook (moe_debug_next_grouped_mlp_silent_token_tile); consumed and
+// cleared by the next fused bf16 grouped-MLP launch of this host thread.
+int64_t take_debug_mlp_silent_tile();
+void set_debug_mlp_silent_tile(int64_t token_tile);
 void set_profile_events(const ProfileEvents& ev);
 
 }  // namespace moe

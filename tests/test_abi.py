@@ -179,3 +179,11 @@ def test_ring_rotation_and_lifetime_errors(moe):
     r.close()
     with pytest.raises(moe.MoeError):
         moe.Ring(0, use_events=False)
+
+
+def test_debug_hook_arguments(moe):
+    """The fused-MLP testing hook takes a token tile or -1 (cancel); anything
+    below -1 is rejected on the host."""
+    moe.moe_debug_next_grouped_mlp_silent_token_tile(-1)
+    with pytest.raises(moe.MoeError):
+        moe.moe_debug_next_grouped_mlp_silent_token_tile(-2)
