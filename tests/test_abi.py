@@ -76,11 +76,12 @@ def test_workspace_queries(moe):
 
 
 def test_grouped_mlp_kernel_count(moe):
-    """bf16 on single SMs is one fused FC1 + FC2 kernel; SM pairs (>= 2048 rows
-    per expert on average), FP8 and NVFP4 launch FC1 and FC2 separately."""
+    """bf16 on single SMs is one fused FC1 + FC2 kernel; SM pairs (>= 4096
+    capacity rows per expert), FP8 and NVFP4 launch FC1 and FC2 separately."""
     s = moe.Shape(T=4096, H=2048, E=64, K=8, I=1024)
     assert moe.moe_grouped_mlp_kernel_count(s, moe.Layout(128, 49152), moe.DTYPE_BF16) == 1
-    assert moe.moe_grouped_mlp_kernel_count(s, moe.Layout(128, 2048 * 64), moe.DTYPE_BF16) == 2
+    assert moe.moe_grouped_mlp_kernel_count(s, moe.Layout(128, 4096 * 64), moe.DTYPE_BF16) == 2
+    assert moe.moe_grouped_mlp_kernel_count(s, moe.Layout(128, 4095 * 64), moe.DTYPE_BF16) == 1
     assert moe.moe_grouped_mlp_kernel_count(s, moe.Layout(128, 49152), moe.DTYPE_FP8_E4M3_B128) == 2
     assert moe.moe_grouped_mlp_kernel_count(s, moe.Layout(128, 49152), moe.DTYPE_NVFP4) == 2
     assert moe.moe_grouped_mlp_kernel_count(s, moe.Layout(128, 0), moe.DTYPE_BF16) == 0

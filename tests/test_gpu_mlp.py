@@ -48,8 +48,8 @@ def run_layer_bf16(moe, w, seed, cap=None, routing=None):
     ("one_expert", _case("tiny", T=300, H=256, E=1, K=1, I=256)),
     ("m1_no_padding", _case("tiny", T=257, H=256, E=7, K=3, I=128, m=1)),
     ("many_experts_pad8", _case("tiny", T=1024, H=512, E=24, K=3, I=256, m=8)),
-    ("pair_large_experts", _case("tiny", T=2048, H=512, E=2, K=2, I=256)),
-    ("pair_ragged_h384", _case("tiny", T=4200, H=384, E=4, K=2, I=128)),
+    ("pair_large_experts", _case("tiny", T=4160, H=512, E=2, K=2, I=256)),
+    ("pair_ragged_h384", _case("tiny", T=8400, H=384, E=4, K=2, I=128)),
 ], ids=lambda v: v if isinstance(v, str) else "")
 def test_grouped_mlp_bf16_all_rows(oracle, moe, name, w):
     r = run_layer_bf16(moe, w, seed=21)
