@@ -13,7 +13,7 @@ namespace moe {
 // kPreMaxEntries routes and at most kPreStageBytes bytes of routing map.
 constexpr int kPreMaxEntries = 4096;
 constexpr int kPreStageBytes = 32768;
-constexpr int kPreTargetTiles = 256;
+constexpr int kPreTargetTiles = 64;
 constexpr int kPreThreads = 256;
 constexpr int kPreWarps = kPreThreads / 32;
 
