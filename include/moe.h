@@ -250,8 +250,10 @@ MOE_API moe_status moe_combine_unpermute(const moe_handle_dev* handle, const moe
 
 /* ------------------------------------------------------------ grouped MLP */
 
-/* Device workspace bytes of moe_grouped_mlp (the intermediate activation
- * [cap][I] in the FC2 input format, plus its scales). */
+/* Device workspace bytes of moe_grouped_mlp: the intermediate activation
+ * [cap][I] in the FC2 input format, plus its scales, plus (bf16 path) a tile
+ * claim counter and one completion counter per token tile, which each call
+ * zeroes itself.  Calls that share a workspace must not overlap on the GPU. */
 MOE_API moe_status moe_grouped_mlp_workspace_size(const moe_shape* shape, const moe_layout* layout,
                                           int32_t w_dtype, size_t* bytes_out);
 
