@@ -189,6 +189,14 @@ class Problem:
         self.yp = torch.empty(cap, dtype=torch.float32, device=dev)
         self.out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
         self.out_host = torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory()
+        # slot 1 of the double-buffered end-to-end pipeline: its own inputs and output
+        map1, probs1 = torch.empty_like(self.map), torch.empty_like(self.probs)
+        self.slots = [
+            dict(x=self.x, map=self.map, probs=self.probs, routing=self.routing, out=self.out,
+                 out_host=self.out_host),
+            dict(x=torch.empty_like(self.x), map=map1, probs=probs1, routing=moe.Routing(fmt, map1, probs1),
+                 out=torch.empty_like(self.out), out_host=torch.empty_like(self.out_host).pin_memory()),
+        ]
         self.globals = None
         self.x_scales = None
         if not self.identity:
@@ -223,21 +231,22 @@ class Problem:
             self.mlp_kernels = moe.moe_grouped_mlp_kernel_count(self.shape, self.layout, self.w_dtype)
         torch.cuda.synchronize()
 
-    def step(self, stream, ev=None, prof=None):
+    def step(self, stream, ev=None, prof=None, slot=0):
         """The four library calls.  ev: events recorded at the call boundaries --
         a list of 5 (before and after every call), or a dict {index: event} for
         a subset of the boundaries 0..4; prof: the grouped-MLP profiling hook's
-        three events."""
+        three events; slot: which input/output buffer set to use."""
         moe = self.moe
+        io = self.slots[slot]
         if isinstance(ev, dict):
             rec = lambda i: ev[i].record(stream) if i in ev else None
         else:
             rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
         rec(0)
-        moe.moe_preprocess(self.routing, self.shape, self.layout, self.handle, self.ws, stream=stream)
+        moe.moe_preprocess(io["routing"], self.shape, self.layout, self.handle, self.ws, stream=stream)
         rec(1)
-        moe.moe_dispatch_permute(self.handle, self.shape, self.layout, self.in_dtype, self.x, self.x_scales,
-                                 self.routing, self.y, self.yp, self.y_scales, stream=stream)
+        moe.moe_dispatch_permute(self.handle, self.shape, self.layout, self.in_dtype, io["x"], self.x_scales,
+                                 io["routing"], self.y, self.yp, self.y_scales, stream=stream)
         rec(2)
         if self.identity:
             expert_out = self.y
@@ -248,7 +257,7 @@ class Problem:
                                 self.w13_s, self.w2, self.w2_s, self.globals, self.act_ws, self.o, stream=stream)
             expert_out = self.o
         rec(3)
-        moe.moe_combine_unpermute(self.handle, self.shape, self.layout, expert_out, self.yp, self.out, stream=stream)
+        moe.moe_combine_unpermute(self.handle, self.shape, self.layout, expert_out, self.yp, io["out"], stream=stream)
         rec(4)
 
     def kernels_per_step(self) -> int:
@@ -382,22 +391,46 @@ def run_ours(args, w):
     t_mlp = mean_ms(2, 3, evs, KB)
     t_com = mean_ms(3, 4, evs, KB)
 
-    # ---- end to end: pinned host inputs in, result out, every step
+    # ---- end to end: every step copies its inputs in from pinned host memory
+    # and its layer output back out.  Two buffer slots and two copy streams let
+    # step i+1's inputs and step i-1's output move while step i computes, as a
+    # serving loop would run it.
     e2e_evs = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     h2d = prob.x_host.numel() * 2 + prob.map_host.numel() * prob.map_host.element_size() + prob.probs_host.numel() * 4
     d2h = prob.out_host.numel() * 2
+    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    compute_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    last_out = torch.cuda.Event()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e2e_evs[0].record(stream)
-        for i in range(K):
-            prob.x.copy_(prob.x_host, non_blocking=True)
-            prob.map.copy_(prob.map_host, non_blocking=True)
-            prob.probs.copy_(prob.probs_host, non_blocking=True)
-            prob.step(stream)
-            prob.out_host.copy_(prob.out, non_blocking=True)
-        e2e_evs[1].record(stream)
+    e2e_evs[0].record(stream)
+    cin.wait_event(e2e_evs[0])
+    for i in range(K):
+        sl = i % 2
+        io = prob.slots[sl]
+        if i >= 2:
+            cin.wait_event(compute_done[sl])  # step i-2 no longer reads this slot's inputs
+        with torch.cuda.stream(cin):
+            io["x"].copy_(prob.x_host, non_blocking=True)
+            io["map"].copy_(prob.map_host, non_blocking=True)
+            io["probs"].copy_(prob.probs_host, non_blocking=True)
+            in_done[sl].record(cin)
+        stream.wait_event(in_done[sl])
+        if i >= 2:
+            stream.wait_event(out_done[sl])  # step i-2's output has left this slot
+        with torch.cuda.stream(stream):
+            prob.step(stream, slot=sl)
+            compute_done[sl].record(stream)
+        cout.wait_event(compute_done[sl])
+        with torch.cuda.stream(cout):
+            io["out_host"].copy_(io["out"], non_blocking=True)
+            out_done[sl].record(cout)
+    last_out.record(cout)
+    stream.wait_event(last_out)
+    e2e_evs[1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e2e_evs[0].elapsed_time(e2e_evs[1]), dev)
 
