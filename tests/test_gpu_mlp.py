@@ -48,6 +48,7 @@ def run_layer_bf16(moe, w, seed, cap=None, routing=None):
     ("one_expert", _case("tiny", T=300, H=256, E=1, K=1, I=256)),
     ("m1_no_padding", _case("tiny", T=257, H=256, E=7, K=3, I=128, m=1)),
     ("many_experts_pad8", _case("tiny", T=1024, H=512, E=24, K=3, I=256, m=8)),
+    ("max_experts_1024", _case("tiny", T=600, H=128, E=1024, K=2, I=128, m=8)),
     ("pair_large_experts", _case("tiny", T=4160, H=512, E=2, K=2, I=256)),
     ("pair_ragged_h384", _case("tiny", T=8400, H=384, E=4, K=2, I=128)),
 ], ids=lambda v: v if isinstance(v, str) else "")
@@ -211,3 +212,46 @@ def test_whole_layer_in_one_cuda_graph(oracle, moe):
         o_full[:v] = ob
         o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"], po)
         assert layer_rel_err(oracle.bf16_to_f64(bits(out)), oracle.bf16_to_f64(ref), o_rows, wts) <= TOL_BF16
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_zero_token_layer(moe, dtype):
+    """T = 0: all four calls run (the grouped MLP claims no tiles), the status
+    word stays clear and nothing is written."""
+    w = _case("tiny", T=0, H=256, E=8, K=2, I=128)
+    cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
+    fmt, rmap, probs = workloads.routing_inputs(w, seed=1)
+    shape, layout, routing_t, handle, _ = preprocess(moe, w, fmt, rmap, probs, cap)
+    rows = max(cap, 1)
+    if dtype == "bf16":
+        w13, w2 = workloads.expert_weights(w, 1, device="cuda")
+        y = fill_pattern(torch.empty(rows, w.H, dtype=torch.bfloat16, device="cuda"))
+        ys = None
+        wd, w13_s, w2_s, in_dtype = moe.DTYPE_BF16, None, None, moe.DTYPE_BF16
+        x = torch.empty(1, w.H, dtype=torch.bfloat16, device="cuda")
+    else:
+        w13b, w2b = workloads.expert_weights(w, 1, device="cuda")
+        w13 = torch.empty(w13b.shape, dtype=torch.uint8, device="cuda")
+        w2 = torch.empty(w2b.shape, dtype=torch.uint8, device="cuda")
+        w13_s = torch.empty(w.E, 2 * w.I // 128, w.H // 128, dtype=torch.float32, device="cuda")
+        w2_s = torch.empty(w.E, w.H // 128, w.I // 128, dtype=torch.float32, device="cuda")
+        moe.moe_quantize_fp8_blocks(w13b, w13, w13_s)
+        moe.moe_quantize_fp8_blocks(w2b, w2, w2_s)
+        y = fill_pattern(torch.empty(rows, w.H, dtype=torch.uint8, device="cuda"))
+        ys = torch.empty(rows, w.H // 128, dtype=torch.float32, device="cuda")
+        wd, in_dtype = moe.DTYPE_FP8_E4M3_B128, moe.DTYPE_BF16_TO_FP8
+        x = torch.empty(1, w.H, dtype=torch.bfloat16, device="cuda")
+    yp = torch.empty(rows, dtype=torch.float32, device="cuda")
+    moe.moe_dispatch_permute(handle, shape, layout, in_dtype, x, None, routing_t, y, yp, ys)
+    ws = torch.empty(max(moe.moe_grouped_mlp_workspace_size(shape, layout, wd), 256), dtype=torch.uint8,
+                     device="cuda")
+    o = fill_pattern(torch.empty(rows, w.H, dtype=torch.bfloat16, device="cuda"))
+    before = bits(o).copy()
+    moe.moe_grouped_mlp(handle, shape, layout, wd, y, ys, w13, w13_s, w2, w2_s, None, ws, o)
+    out = fill_pattern(torch.empty(1, w.H, dtype=torch.bfloat16, device="cuda"))
+    moe.moe_combine_unpermute(handle, shape, layout, o, yp, out)
+    torch.cuda.synchronize()
+    assert int(handle.status.item()) == 0
+    assert int(handle.total_rows.item()) == 0
+    # every expert segment is empty, so no expert row is written
+    assert np.array_equal(bits(o), before)
