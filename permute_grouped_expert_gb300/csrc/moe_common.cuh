@@ -26,12 +26,6 @@ MOE_DEVICE uint64_t globaltimer_ns() {
   return t;
 }
 
-MOE_DEVICE uint64_t ld_acquire_u64(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
 MOE_DEVICE void st_release_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
