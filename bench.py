@@ -321,10 +321,11 @@ def run_ours(args, w):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl", init_method="env://")
+    # the device first, so that NCCL's communicator and every barrier use this rank's GPU
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
     if rank == 0 or world == 1:
         __graft_entry__.build_library()
     if world > 1:
