@@ -45,7 +45,8 @@ struct PreParams {
   int32_t* slot_of;
   int32_t* total_rows;
   int32_t* overflow;
-  int32_t* status;
+  int32_t* status;      // the handle's status word: written once, by the finalize kernel
+  int32_t* ws_status;   // this call's status bits, gathered in the workspace (cleared with the counters)
   int64_t silent_tile;  // testing hook: this tile never publishes its lookback words (-1: none)
 };
 
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
   }
   if (err) atomicOr(&s_err, err);
   __syncthreads();
-  if (tid == 0 && s_err) set_status(p.status, s_err);
+  if (tid == 0 && s_err) set_status(p.ws_status, s_err);
 
   // warp bases and tile aggregate per expert; publish the aggregate at once
   for (int e = tid; e < E; e += blockDim.x) {
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
           if (stop > 0 || t_start == 0) {
             t_start = now;
           } else if (now - t_start > kWaitLimitNs) {
-            set_status(p.status, MOE_DEV_ERR_TIMEOUT);
+            set_status(p.ws_status, MOE_DEV_ERR_TIMEOUT);
             break;
           }
           __nanosleep(32);
@@ -316,6 +317,8 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
 __global__ void __launch_bounds__(256) pre_finalize_kernel(PreParams p) {
   extern __shared__ __align__(16) int32_t soff[];  // [E+1]
   const int E = (int)p.E;
+  // the rank kernel has finished: its status bits replace the handle's status word
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = *p.ws_status;
   for (int i = threadIdx.x; i <= E; i += blockDim.x) soff[i] = p.offsets[i];
   __syncthreads();
   const int64_t n = p.T * p.K;
@@ -388,10 +391,10 @@ cudaError_t launch_preprocess(const moe_routing& r, const moe_shape& s, const mo
   p.total_rows = h.total_rows;
   p.overflow = h.overflow;
   p.status = h.status;
+  p.ws_status = ws.tile_counter + 32;  // inside the cleared header, 128 bytes after the tile counter
 
   cudaError_t e;
   if ((e = cudaMemsetAsync(ws.tile_counter, 0, ws.memset_bytes, st)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(h.status, 0, sizeof(int32_t), st)) != cudaSuccess) return e;
 
   const size_t smem_a = (size_t)(kPreWarps + 2) * s.E * 4 + (size_t)kPreMaxEntries * 6 + kPreStageBytes;
   static bool attr_done = false;
