@@ -25,7 +25,7 @@
 //   warps 2..9  converters: E2M1 + E4M3 -> f16, written in the 128-byte swizzled
 //               K-major layout the MMA reads, 64 K elements per converted stage;
 //               each thread expands half a weight row (plus, for 64 threads, half
-//               a token row)
+//               a token row; token rows past the expert's end are skipped)
 //   warps 10..13 epilogue: FC1 exchanges gate rows through shared memory, applies
 //               SwiGLU and re-encodes the intermediate to NVFP4; FC2 writes bf16.
 // Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit).
@@ -330,11 +330,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- converters
     const int c = threadIdx.x - 64;  // 0..255: weight row c & 127, half c >> 7
     const int wrow = c & 127, whalf = c >> 7;
-    const int xrow = c & 31, xhalf = (c >> 5) & 1;  // token half-rows for c < 64
+    const int xrow = c >> 1, xhalf = c & 1;  // token half-rows for c < 64: rows 0..15 in warp 2
     int rst = 0, cst = 0;
     uint32_t rphase = 0, cphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      // Token rows past the expert's end are not converted: the accumulator
+      // column of a token row depends on that row alone, and the epilogue stores
+      // valid rows only, so whatever those columns of the converted stage hold
+      // never reaches the output.  Whole warps skip when their rows are all past it.
+      const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
+      const bool x_conv = c < 2 * BNT && (int64_t)xrow < ti.row_end - ti.row0;
       for (int kr = 0; kr < p.nkr && ok; kr++) {
         int w_ok = 0;
         if (lane == 0) w_ok = mbar_wait(&s_rfull[rst], rphase, abort_flag, p.status) ? 1 : 0;
@@ -355,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* cs = cvt + (size_t)cst * kCvtStride;
           convert_half_row(st + wrow * (BKR / 2), wrow, s, whalf, st + kRawW + wrow * (BKR / 16),
                            cs + wrow * (BKC * 2));
-          if (c < 2 * BNT)
+          if (x_conv)
             convert_half_row(st + kRawW + kRawWS + xrow * (BKR / 2), xrow, s, xhalf,
                              st + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2));
           // make the generic-proxy stores visible to the tensor cores, then publish
@@ -425,8 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q < 2) {
           const float g2 = *p.out_global;
           const int64_t col = (int64_t)ti.mt * 64 + wr;  // intermediate column of this thread
-#pragma unroll 4
+          const int64_t nvalid = ti.row_end - ti.row0;    // token columns of this tile that exist
+#pragma unroll
           for (int j = 0; j < BNT; j++) {
+            if (j >= nvalid) break;  // warp-uniform
             const float gt = gbuf[wr][j];
             const float a = gt / (1.0f + __expf(-gt)) * (alpha * v[j]);
             // NVFP4 block = 16 consecutive columns = 16 consecutive lanes
@@ -437,13 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float denom = e4m3_to_float(scode) * g2;
             const float partner = __shfl_xor_sync(0xffffffffu, a, 1);
             const int64_t row = ti.row0 + j;
-            if (row < ti.row_end) {
-              if ((lane & 1) == 0) {
-                const uint32_t b = (denom == 0.0f) ? 0u : e2m1x2(__fdiv_rn(a, denom), __fdiv_rn(partner, denom));
-                p.out[row * (p.ld_out / 2) + col / 2] = (uint8_t)b;
-              }
-              if ((lane & 15) == 0) p.out_scales[row * (p.ld_out / 16) + col / 16] = (uint8_t)scode;
+            if ((lane & 1) == 0) {
+              const uint32_t b = (denom == 0.0f) ? 0u : e2m1x2(__fdiv_rn(a, denom), __fdiv_rn(partner, denom));
+              p.out[row * (p.ld_out / 2) + col / 2] = (uint8_t)b;
             }
+            if ((lane & 15) == 0) p.out_scales[row * (p.ld_out / 16) + col / 16] = (uint8_t)scode;
           }
         }
       }
