@@ -20,10 +20,11 @@
 // One CTA per SM, 14 warps:
 //   warp 0      TMA producer: raw stages of 256 K elements (packed weights
 //               128 rows x 128 B, their scales 128 x 16 B, packed tokens 32 x 128 B,
-//               their scales 32 x 16 B), 5 stages
+//               their scales 32 x 16 B), 4 stages
 //   warp 1      TMEM allocation (2 x 32 fp32 columns) and MMA issue
 //   warps 2..9  converters: E2M1 + E4M3 -> f16, written in the 128-byte swizzled
-//               K-major layout the MMA reads, 64 K elements per converted stage;
+//               K-major layout the MMA reads, 64 K elements per converted stage
+//               (5 stages);
 //               each thread expands half a weight row (plus, for 64 threads, half
 //               a token row; token rows past the expert's end are skipped)
 //   warps 10..13 epilogue: FC1 exchanges gate rows through shared memory, applies
@@ -43,8 +44,8 @@ constexpr int BMW = 128;        // weight rows per tile (MMA M)
 constexpr int BNT = 32;         // tokens per tile (MMA N)
 constexpr int BKR = 256;        // K elements per raw stage
 constexpr int BKC = 64;         // K elements per converted stage
-constexpr int kRawStages = 5;
-constexpr int kCvtStages = 3;
+constexpr int kRawStages = 4;
+constexpr int kCvtStages = 5;
 constexpr int kCvtWarps = 8;
 constexpr int kThreads = 64 + 32 * kCvtWarps + 128;
 constexpr uint32_t kRawW = BMW * (BKR / 2);        // 16 KB packed weights
