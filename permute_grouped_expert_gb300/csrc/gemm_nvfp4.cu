@@ -69,12 +69,6 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-MOE_DEVICE uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
-  return r;
-}
-
 MOE_DEVICE uint32_t e4m3_pair_to_f16x2(uint32_t code) {
   uint32_t r;
   const uint16_t pair = (uint16_t)(code | (code << 8));
@@ -86,6 +80,22 @@ MOE_DEVICE uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
+}
+
+// Eight packed E2M1 elements -> four f16x2 words (element pairs in order); the
+// word is split into its bytes by one vector move so each convert reads a byte
+// register directly.
+MOE_DEVICE uint4 e2m1x8_to_f16x8(uint32_t w) {
+  uint4 o;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
+      : "r"(w));
+  return o;
 }
 
 struct Fp4Params {
@@ -142,11 +152,11 @@ __device__ __forceinline__ void convert_half_row(const uint8_t* raw_row_base, in
 #pragma unroll
     for (int i = 0; i < 2; i++) {  // one 16-byte output chunk = 8 elements = 4 packed bytes
       const uint32_t w = words[2 * g + i];
-      uint4 o;
-      o.x = hmul2(e2m1x2_to_f16x2(w & 0xffu), sh);
-      o.y = hmul2(e2m1x2_to_f16x2((w >> 8) & 0xffu), sh);
-      o.z = hmul2(e2m1x2_to_f16x2((w >> 16) & 0xffu), sh);
-      o.w = hmul2(e2m1x2_to_f16x2(w >> 24), sh);
+      uint4 o = e2m1x8_to_f16x8(w);
+      o.x = hmul2(o.x, sh);
+      o.y = hmul2(o.y, sh);
+      o.z = hmul2(o.z, sh);
+      o.w = hmul2(o.w, sh);
       const int chunk = 4 * h + 2 * g + i;
       *reinterpret_cast<uint4*>(cvt_row_base + ((chunk ^ sw) << 4)) = o;
     }
