@@ -476,7 +476,8 @@ def run_ours(args, w):
                               "fc2_weight_gbs": round(prob.fc2_bytes(R, active) / (t_fc2 * 1e-3) / 1e9, 1)})
             roof = {"kernel": "grouped_fc1_swiglu (NVFP4)", "bound": "hbm", "achieved": round(achieved_gbs, 1),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
-                    "traffic": None, "peak_source": f"{peak_src} hbm_gbs"}
+                    "traffic": profiled_traffic(w.name, "permute_grouped_expert_gb300/csrc/gemm_nvfp4.cu"),
+                    "peak_source": f"{peak_src} hbm_gbs"}
             kernel = None
         else:
             achieved = prob.fc1_flops(R) / (t_fc1 * 1e-3) / 1e12
