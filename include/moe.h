@@ -122,7 +122,8 @@ typedef struct moe_shape {
 } moe_shape;
 
 typedef struct moe_layout {
-  int64_t pad_multiple; /* m: each expert's segment is padded to a multiple of m (>= 1) */
+  int64_t pad_multiple; /* m: each expert's segment is padded to a multiple of m (>= 1);
+                           T*K + E*(m-1), the largest padded total, must be < 2^31 */
   int64_t capacity;     /* cap: rows of the dispatch / expert-output buffers (>= 0).
                            Routes whose destination row reaches cap are dropped. */
 } moe_layout;
@@ -194,12 +195,17 @@ MOE_API moe_status moe_preprocess(const moe_routing* routing, const moe_shape* s
  * the library (MOE_PREPROCESS_NOALLOC_SCRATCH_BYTES, held by every GPU that
  * loads the library until the process exits) instead of a caller workspace.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
- *   - Shapes whose scratch need (moe_preprocess_workspace_size) exceeds
+ *   - Checks, in order: the arguments as moe_preprocess checks them
+ *     (MOE_ERR_INVALID_ARG), then the size rule: shapes whose scratch need
+ *     (moe_preprocess_workspace_size) exceeds
  *     MOE_PREPROCESS_NOALLOC_SCRATCH_BYTES are rejected with
- *     MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
- *   - The first call on a device (with that device current) looks up the
- *     array's device address with cudaGetSymbolAddress and caches it; make
- *     that first call before any stream capture.
+ *     MOE_ERR_WORKSPACE_TOO_SMALL.  Nothing is enqueued when a check fails.
+ *   - Each call outside stream capture looks up the array's device address
+ *     on the current device with cudaGetSymbolAddress (so a module reloaded
+ *     after cudaDeviceReset is found at its new address) and caches it per
+ *     device; a call made during stream capture uses that cached address.
+ *     Make at least one call on a device before capturing on it, and none
+ *     between a cudaDeviceReset and the next uncaptured call.
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents; each call clears the bytes that must start at zero on
  *     its own stream.  Calls whose GPU work overlaps (other streams, other host

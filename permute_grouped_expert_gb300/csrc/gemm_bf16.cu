@@ -503,13 +503,12 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
   if ((e = make_tensor_map_2d(&tw2, w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)s.E * s.H, s.I, BW, BK)) !=
       cudaSuccess)
     return e;
-  static bool attr = false;
-  if (!attr) {
-    if ((e = cudaFuncSetAttribute(grouped_mlp_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kDynSmem)) != cudaSuccess)
-      return e;
-    attr = true;
-  }
+  static PerDeviceOnce attr_once;
+  if ((e = attr_once.run([] {
+         return cudaFuncSetAttribute(grouped_mlp_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kDynSmem);
+       })) != cudaSuccess)
+    return e;
   const size_t ready_bytes = grouped_mlp_bf16_ready_bytes(s, l);
   if ((e = cudaMemsetAsync(ready, 0, ready_bytes, st)) != cudaSuccess) return e;
 

@@ -330,13 +330,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <int kMode>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const PairParams& p, int64_t max_tiles,
                         cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_bf16_pair_kernel<kMode>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce attr_once;
+  cudaError_t e = attr_once.run([] {
+    return cudaFuncSetAttribute(grouped_gemm_bf16_pair_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+  });
+  if (e != cudaSuccess) return e;
   int64_t clusters = device_sm_count() / 2;
   if (clusters > max_tiles) clusters = max_tiles;
   if (clusters < 1) clusters = 1;

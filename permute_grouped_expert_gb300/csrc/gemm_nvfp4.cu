@@ -478,13 +478,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int kMode>
 cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tws, const CUtensorMap& tx, const CUtensorMap& txs,
                        const Fp4Params& p, int64_t max_tiles, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<kMode>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce attr_once;
+  cudaError_t e = attr_once.run([] {
+    return cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+  });
+  if (e != cudaSuccess) return e;
   int64_t grid = device_sm_count();
   if (grid > max_tiles) grid = max_tiles;
   if (grid < 1) grid = 1;

@@ -8,6 +8,12 @@
 
 #include "moe_internal.h"
 
+#define MOE_TRY_INTERNAL(expr)          \
+  do {                                   \
+    moe_status _st = (expr);             \
+    if (_st != MOE_OK) return _st;       \
+  } while (0)
+
 namespace moe {
 
 namespace {
@@ -29,8 +35,16 @@ moe_status check_shape(const moe_shape* s, bool need_h) {
 }
 
 moe_status check_layout(const moe_layout* l) {
-  if (!l || l->pad_multiple < 1 || l->capacity < 0 || l->capacity >= (int64_t(1) << 31))
+  if (!l || l->pad_multiple < 1 || l->pad_multiple >= (int64_t(1) << 31) || l->capacity < 0 ||
+      l->capacity >= (int64_t(1) << 31))
     return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// The padded total sum_e ceil(count[e]/m)*m is at most T*K + E*(m-1); offsets,
+// total_rows and row ids are int32, so that bound must stay below 2^31.
+moe_status check_padded_total(const moe_shape* s, const moe_layout* l) {
+  if (s->T * s->K + s->E * (l->pad_multiple - 1) >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -53,6 +67,16 @@ thread_local ProfileEvents g_profile;
 }
 
 void record_cuda_error(cudaError_t e) { cuda_fail(e); }
+
+moe_status validate_preprocess_args(const moe_routing* routing, const moe_shape* shape, const moe_layout* layout,
+                                    const moe_handle_dev* handle) {
+  MOE_TRY_INTERNAL(check_shape(shape, false));
+  MOE_TRY_INTERNAL(check_routing(routing, shape->T));
+  MOE_TRY_INTERNAL(check_layout(layout));
+  MOE_TRY_INTERNAL(check_padded_total(shape, layout));
+  MOE_TRY_INTERNAL(check_handle(handle));
+  return MOE_OK;
+}
 
 ProfileEvents take_profile_events() {
   ProfileEvents e = g_profile;
@@ -142,6 +166,7 @@ moe_status moe_preprocess(const moe_routing* routing, const moe_shape* shape, co
   MOE_TRY(check_shape(shape, false));
   MOE_TRY(check_routing(routing, shape->T));
   MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
   MOE_TRY(check_handle(handle));
   if (!workspace || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < preprocess_workspace_bytes(shape->T, shape->E, shape->K))
@@ -157,6 +182,7 @@ moe_status moe_debug_preprocess_silent_tile(const moe_routing* routing, const mo
   MOE_TRY(check_shape(shape, false));
   MOE_TRY(check_routing(routing, shape->T));
   MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
   MOE_TRY(check_handle(handle));
   if (!workspace || !aligned16(workspace) || silent_tile < 0) return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < preprocess_workspace_bytes(shape->T, shape->E, shape->K))
@@ -174,6 +200,7 @@ moe_status moe_dispatch_permute(const moe_handle_dev* handle, const moe_shape* s
   MOE_TRY(check_handle(handle));
   MOE_TRY(check_shape(shape, true));
   MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
   MOE_TRY(check_routing(routing, shape->T));
   if ((shape->T > 0 && !x) || !out_tokens || !aligned16(x) || !aligned16(out_tokens))
     return MOE_ERR_INVALID_ARG;
@@ -203,6 +230,7 @@ moe_status moe_combine_unpermute(const moe_handle_dev* handle, const moe_shape* 
   MOE_TRY(check_handle(handle));
   MOE_TRY(check_shape(shape, true));
   MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
   if (!expert_out || (shape->T > 0 && !y) || !aligned16(expert_out) || !aligned16(y))
     return MOE_ERR_INVALID_ARG;
   cudaError_t e = launch_combine(*handle, *shape, *layout, expert_out, perm_probs, y,
@@ -214,6 +242,7 @@ moe_status moe_grouped_mlp_workspace_size(const moe_shape* shape, const moe_layo
                                           int32_t w_dtype, size_t* bytes_out) {
   MOE_TRY(check_shape(shape, true));
   MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
   if (!bytes_out || shape->I <= 0 || shape->I % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (w_dtype != MOE_DTYPE_BF16 && w_dtype != MOE_DTYPE_FP8_E4M3_B128 && w_dtype != MOE_DTYPE_NVFP4)
     return MOE_ERR_INVALID_ARG;
@@ -225,6 +254,7 @@ moe_status moe_grouped_mlp_kernel_count(const moe_shape* shape, const moe_layout
                                         int32_t* count_out) {
   MOE_TRY(check_shape(shape, true));
   MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
   if (!count_out || shape->I <= 0 || shape->I % 128 != 0) return MOE_ERR_INVALID_ARG;
   const int n = grouped_mlp_kernel_count(*shape, *layout, w_dtype);
   if (n < 0) return MOE_ERR_INVALID_ARG;
@@ -240,6 +270,7 @@ moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape,
   MOE_TRY(check_handle(handle));
   MOE_TRY(check_shape(shape, true));
   MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
   if (shape->I <= 0 || shape->I % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (!perm_tokens || !w13 || !w2 || !out_fc2 || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned16(perm_tokens) || !aligned16(w13) || !aligned16(w2) || !aligned16(out_fc2) ||

@@ -5,6 +5,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "moe.h"
 
 namespace moe {
@@ -67,6 +70,37 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                void* workspace, void* out_fc2, cudaStream_t st);
 
 int device_sm_count();
+
+// Runs a per-device setup step (a kernel attribute such as its dynamic
+// shared-memory limit, which CUDA keeps per device) once for each device it is
+// called on, with that device current.  Thread-safe; a failed step is retried
+// on the next call.
+class PerDeviceOnce {
+ public:
+  static constexpr int kMaxDevices = 64;
+  template <class F>
+  cudaError_t run(F&& step) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mutex_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = step();
+    if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::mutex mutex_;
+  std::atomic<bool> done_[kMaxDevices] = {};
+};
+
+// Host-side argument checks of moe_preprocess (shape, routing, layout, padded
+// total, handle), in that order; MOE_OK or MOE_ERR_INVALID_ARG.
+moe_status validate_preprocess_args(const moe_routing* routing, const moe_shape* shape, const moe_layout* layout,
+                                    const moe_handle_dev* handle);
 
 // Records a CUDA error for moe_last_cuda_error() (the caller returns MOE_ERR_CUDA).
 void record_cuda_error(cudaError_t e);

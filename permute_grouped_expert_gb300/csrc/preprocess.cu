@@ -211,10 +211,10 @@ __global__ void __launch_bounds__(kPreThreads) pre_rank_kernel(PreParams p) {
     }
     agg[e] = s;
     uint64_t* word = p.lookback + tile * p.E + e;
+    if (tile == 0) prefix[e] = 0;  // set even when the tile stays silent: the rank loop reads it
     if (tile == p.silent_tile) {
       // testing hook: successors find nothing published and their bounded wait runs out
     } else if (tile == 0) {
-      prefix[e] = 0;
       st_release_u64(word, kFlagInclusive | (uint32_t)s);
     } else {
       st_release_u64(word, kFlagAggregate | (uint32_t)s);
@@ -318,7 +318,11 @@ __global__ void __launch_bounds__(256) pre_finalize_kernel(PreParams p) {
   extern __shared__ __align__(16) int32_t soff[];  // [E+1]
   const int E = (int)p.E;
   // the rank kernel has finished: its status bits replace the handle's status word
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = *p.ws_status;
+  const int32_t ws_status = *p.ws_status;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = ws_status;
+  // after a timed-out lookback the ranks and offsets are incomplete: every route is
+  // marked dropped and nothing is scattered (the call's outputs are documented invalid)
+  const bool valid = (ws_status & MOE_DEV_ERR_TIMEOUT) == 0;
   for (int i = threadIdx.x; i <= E; i += blockDim.x) soff[i] = p.offsets[i];
   __syncthreads();
   const int64_t n = p.T * p.K;
@@ -326,9 +330,9 @@ __global__ void __launch_bounds__(256) pre_finalize_kernel(PreParams p) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const int e = p.route_expert[i];
     int32_t out = -1;
-    if (e >= 0) {
+    if (valid && e >= 0) {
       const int64_t dest = (int64_t)soff[e] + p.row_of[i];
-      if (dest < p.cap) {
+      if (dest >= 0 && dest < p.cap) {
         out = (int32_t)dest;
         p.token_of[dest] = (int32_t)(i / p.K);
         p.slot_of[dest] = (int32_t)(i % p.K);
@@ -337,8 +341,9 @@ __global__ void __launch_bounds__(256) pre_finalize_kernel(PreParams p) {
     p.row_of[i] = out;
   }
   // pad rows of each expert segment (fewer than m per expert)
+  if (!valid) return;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E; e += stride) {
-    const int64_t beg = (int64_t)soff[e] + p.counts[e];
+    const int64_t beg = max64(0, (int64_t)soff[e] + p.counts[e]);
     const int64_t end = min64(soff[e + 1], p.cap);
     for (int64_t r = beg; r < end; r++) {
       p.token_of[r] = -1;
@@ -397,13 +402,12 @@ cudaError_t launch_preprocess(const moe_routing& r, const moe_shape& s, const mo
   if ((e = cudaMemsetAsync(ws.tile_counter, 0, ws.memset_bytes, st)) != cudaSuccess) return e;
 
   const size_t smem_a = (size_t)(kPreWarps + 2) * s.E * 4 + (size_t)kPreMaxEntries * 6 + kPreStageBytes;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if ((e = cudaFuncSetAttribute(pre_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)((kPreWarps + 2) * 1024 * 4 + kPreMaxEntries * 6 + kPreStageBytes))) != cudaSuccess)
-      return e;
-    attr_done = true;
-  }
+  static PerDeviceOnce attr_once;
+  e = attr_once.run([] {
+    return cudaFuncSetAttribute(pre_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)((kPreWarps + 2) * 1024 * 4 + kPreMaxEntries * 6 + kPreStageBytes));
+  });
+  if (e != cudaSuccess) return e;
   pre_rank_kernel<<<(unsigned)p.num_tiles, kPreThreads, smem_a, st>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

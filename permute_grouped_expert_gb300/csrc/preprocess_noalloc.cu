@@ -27,15 +27,20 @@ static __device__ __align__(256) unsigned char g_preprocess_scratch[kNoAllocScra
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached.
-cudaError_t scratch_for_current_device(void** out) {
+// Device address of the scratch array on the current device.  Outside stream
+// capture it is looked up afresh (with the device current), so a module that
+// was reloaded after cudaDeviceReset gives its new address; during capture the
+// address cached by the last lookup on this device is used, because a capture
+// must not depend on a call that may load the module.
+cudaError_t scratch_for_current_device(cudaStream_t stream, void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(stream, &cap)) != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone || !g_scratch_ptr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_preprocess_scratch);
     if (e != cudaSuccess) return e;
@@ -52,17 +57,19 @@ cudaError_t scratch_for_current_device(void** out) {
 extern "C" moe_status moe_preprocess_noalloc(const moe_routing* routing, const moe_shape* shape,
                                              const moe_layout* layout, const moe_handle_dev* handle,
                                              void* stream) {
-  size_t need = 0;
-  moe_status st = moe_preprocess_workspace_size(shape, &need);
+  // Argument checks first (as moe_preprocess makes them), then the size rule.
+  moe_status st = moe::validate_preprocess_args(routing, shape, layout, handle);
   if (st != MOE_OK) return st;
+  size_t need = 0;
+  if ((st = moe_preprocess_workspace_size(shape, &need)) != MOE_OK) return st;
   if (need > moe::kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;  // shape beyond the fixed scratch
   void* scratch = nullptr;
-  cudaError_t e = moe::scratch_for_current_device(&scratch);
+  cudaError_t e = moe::scratch_for_current_device(static_cast<cudaStream_t>(stream), &scratch);
   if (e != cudaSuccess) {
     moe::record_cuda_error(e);
     return MOE_ERR_CUDA;
   }
-  // The ordinary entry point validates the arguments, clears the scratch bytes
-  // that must start at zero (on `stream`) and launches the same kernels.
+  // The ordinary entry point clears the scratch bytes that must start at zero
+  // (on `stream`) and launches the same kernels.
   return moe_preprocess(routing, shape, layout, handle, scratch, moe::kNoAllocScratchBytes, stream);
 }

@@ -101,6 +101,7 @@ def test_validation_rejects_before_any_launch(moe):
     good_layout = moe._Layout(32, 1024)
     routing = moe._Routing(0, fake, None)
     handle = moe._HandleDev(*([fake] * 8))
+    h_missing = moe._HandleDev(*([fake] * 7 + [None]))
     byref = ctypes.byref
     lib = moe.library()
     # null routing map
@@ -117,6 +118,19 @@ def test_validation_rejects_before_any_launch(moe):
                               1 << 30, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_preprocess(byref(routing), byref(good_shape), byref(moe._Layout(0, 10)), byref(handle), fake,
                               1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    # a pad multiple whose largest padded total T*K + E*(m-1) does not fit int32 row ids
+    assert lib.moe_preprocess(byref(routing), byref(good_shape), byref(moe._Layout(1 << 28, 1024)), byref(handle),
+                              fake, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_preprocess(byref(routing), byref(good_shape), byref(moe._Layout(1 << 40, 1024)), byref(handle),
+                              fake, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_permute(byref(handle), byref(good_shape), byref(moe._Layout(1 << 28, 1024)),
+                                    moe.DTYPE_BF16, fake, None, byref(routing), fake, None, None,
+                                    None) == moe.MOE_ERR_INVALID_ARG
+    # the same checks come before the size rule of the allocation-free entry point
+    assert lib.moe_preprocess_noalloc(byref(routing), byref(moe._Shape(1 << 22, 128, 64, 8, 0)),
+                                      byref(moe._Layout(0, 1024)), byref(handle), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_preprocess_noalloc(byref(routing), byref(good_shape), byref(good_layout), byref(h_missing),
+                                      None) == moe.MOE_ERR_INVALID_ARG
     # workspace too small
     assert lib.moe_preprocess(byref(routing), byref(good_shape), byref(good_layout), byref(handle), fake, 16,
                               None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL

@@ -22,7 +22,9 @@ def test_bounded_lookback_wait_reports_timeout_and_context_survives(oracle):
     shape, layout, routing, handle, ws = preprocess(moe, w, fmt, rmap, probs, cap)
     torch.cuda.synchronize()
     t0 = time.time()
-    moe.moe_debug_preprocess_silent_tile(routing, shape, layout, handle, ws, silent_tile=0)
+    # a tile after the first stays silent: its own lookback completes, and every later
+    # tile's wait runs out (tile 0 would publish the chain's first inclusive prefix)
+    moe.moe_debug_preprocess_silent_tile(routing, shape, layout, handle, ws, silent_tile=1)
     torch.cuda.synchronize()
     elapsed = time.time() - t0
     status = int(handle.status.item())

@@ -60,13 +60,20 @@ def test_noalloc_matches_workspace_entry_point_twice(case):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
+    """Only the size rule fails here: the routing, layout and handle are valid
+    device buffers of the oversized shape, so the status names the scratch."""
     moe = moe_mod()
-    big = moe.Shape(T=1 << 22, H=128, E=64, K=8)   # needs far more than the fixed scratch
+    big = moe.Shape(T=1 << 20, H=128, E=64, K=8)   # needs about 17 MiB of scratch
     assert moe.moe_preprocess_workspace_size(big) > 8 << 20
-    layout = moe.Layout(1, 1 << 20)
-    dummy = torch.empty(1, dtype=torch.int32, device="cuda")
-    routing = moe.Routing(moe.ROUTING_DENSE_I16, dummy)
-    handle = moe.Handle(*([dummy] * 8))
+    cap = workloads.unbounded_capacity(big.T, big.K, big.E, 32)
+    layout = moe.Layout(32, cap)
+    rmap = torch.zeros(big.T, big.K, dtype=torch.int16, device="cuda")
+    routing = moe.Routing(moe.ROUTING_DENSE_I16, rmap)
+    handle = moe.Handle.empty(big, layout)
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_preprocess_noalloc(routing, big, layout, handle)
     assert ei.value.status == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    # a malformed argument is reported as such, before the size rule
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_preprocess_noalloc(routing, big, moe.Layout(0, cap), handle)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
