@@ -238,27 +238,46 @@ def test_nvfp4_mlp_single_expert_matches_torch_matmul(oracle):
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-12)
 
 
-@pytest.mark.parametrize("fmt", [0, 1])
+def _nvfp4_per_expert(oracle, wt):
+    """NVFP4 encoding of bf16 expert weights [E][N][K], each expert with its own
+    global scale (amax / (6 * 448), so its largest block scale is E4M3's maximum)."""
+    wf = wt.float().numpy()
+    g = np.array([np.abs(wf[e]).max() / 2688.0 for e in range(wt.shape[0])], np.float32)
+    packs, scs = zip(*[oracle.quantize_nvfp4_rows(_bits(wt[e:e + 1]), float(g[e])) for e in range(wt.shape[0])])
+    return np.concatenate(packs), np.concatenate(scs), g
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_grouped_equals_unpermuted_per_token_layer(oracle, fmt):
     """The whole permuted pipeline equals the per-token formulation bit for bit."""
     w = workloads.scaled(workloads.WORKLOADS["tiny"], T=48, H=256, E=6, K=3, I=128)
     rfmt, rmap, p, cap, pre = _setup(oracle, w, seed=7)
     x = _bits(workloads.activations(w, 7))
     w13, w2 = workloads.expert_weights(w, 7)
+    g13 = g2w = None
+    g1 = g2a = 0.0
     if fmt == 0:
         xa, xsc, a13, s13, a2, s2 = x, None, _bits(w13), None, _bits(w2), None
-    else:
+    elif fmt == 1:
         xa, xsc = oracle.quantize_fp8_rows(x)
         a13, s13 = oracle.quantize_fp8_weight(_bits(w13))
         a2, s2 = oracle.quantize_fp8_weight(_bits(w2))
+    else:
+        g1 = float(np.float32(np.abs(oracle.bf16_to_f64(x)).max() / 2688.0))
+        g2a = 0.004
+        xa, xsc = oracle.quantize_nvfp4_rows(x, g1)
+        a13, s13, g13 = _nvfp4_per_expert(oracle, w13)
+        a2, s2, g2w = _nvfp4_per_expert(oracle, w2)
+    globs = dict(w13_global=g13, w2_global=g2w, fc1_in_global=g1, fc2_in_global=g2a)
     y, yp = oracle.dispatch(rfmt, rmap, p, pre, xa, cap, w.E, w.K)
     ys = oracle.dispatch(rfmt, rmap, None, pre, xsc, cap, w.E, w.K)[0] if xsc is not None else None
     rows = np.arange(pre["valid_rows"])
-    o, _ = oracle.grouped_mlp_rows(fmt, y, ys, w.H, w.I, w.E, pre["offsets"], a13, s13, a2, s2, rows)
+    o, _ = oracle.grouped_mlp_rows(fmt, y, ys, w.H, w.I, w.E, pre["offsets"], a13, s13, a2, s2, rows, **globs)
     out = oracle.combine(o, pre["row_of"], yp)
     ref = oracle.layer_per_token(fmt, rfmt, rmap, p, w.E, w.K, xa, xsc, w.H, w.I, a13, s13, a2, s2,
-                                 np.arange(w.T))
+                                 np.arange(w.T), **globs)
     assert np.array_equal(out, ref)
+    assert np.abs(oracle.bf16_to_f64(out)).max() > 0  # a non-trivial layer
     # pad rows (zero input) give exactly zero output
     for e in range(w.E):
         for r in range(pre["offsets"][e] + pre["counts"][e], pre["offsets"][e + 1]):
@@ -279,3 +298,109 @@ def test_zero_weights_give_zero_output(oracle):
     out, _ = oracle.grouped_mlp_rows(0, x, None, w.H, w.I, 2, np.array([0, 4, 8], np.int32), half, None,
                                      _bits(w2), None, np.arange(8))
     assert not out.any()
+
+
+def _e4m3_round_trip_blocks(a32, block, glob=None):
+    """Re-encode an fp32 intermediate [rows][I] the way the method stores it,
+    using library casts: FP8 (block None) per 1x128 block with scale amax/448;
+    NVFP4 (block 16) with E4M3 block scales under the global scale ``glob``."""
+    import oracle as o
+
+    out = np.zeros(a32.shape, np.float64)
+    if glob is None:
+        for b in range(a32.shape[1] // 128):
+            blk = a32[:, b * 128:(b + 1) * 128]
+            sc = np.abs(blk).max(1).astype(np.float32) / np.float32(448)
+            sc = np.where(sc == 0, np.float32(1), sc)
+            code = torch.from_numpy((blk / sc[:, None]).astype(np.float32)).to(torch.float8_e4m3fn)
+            out[:, b * 128:(b + 1) * 128] = code.double().numpy() * sc[:, None]
+        return out
+    for r in range(a32.shape[0]):
+        for b in range(a32.shape[1] // 16):
+            blk = a32[r, b * 16:(b + 1) * 16]
+            sc = torch.tensor(np.float32(np.abs(blk).max()) / np.float32(6 * np.float32(glob)),
+                              dtype=torch.float32).to(torch.float8_e4m3fn).double().item()
+            den = np.float32(np.float32(sc) * np.float32(glob))
+            codes = o.e2m1_encode((blk / den).astype(np.float32)) if den != 0 else np.zeros(16, np.uint8)
+            out[r, b * 16:(b + 1) * 16] = o.e2m1_decode(codes) * sc * glob
+    return out
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_grouped_mlp_picks_each_experts_own_weights_scales_and_globals(oracle, fmt):
+    """Several experts with different weights (and so different FP8 block scales
+    and NVFP4 global scales), one of them empty: every row's output equals a
+    torch float64 FFN of that row with the slice of its own expert, dequantized
+    by library casts with that expert's scales.  Pins the expert lookup from the
+    offsets, the per-expert weight row offset, the FP8 scale-block index and the
+    per-expert NVFP4 global, none of which a single-expert case exercises."""
+    H, I, E = 256, 128, 4
+    offsets = np.array([0, 6, 12, 12, 18], np.int32)  # expert 2 receives no rows
+    rng = np.random.default_rng(11)
+    y_bf = torch.from_numpy(rng.standard_normal((18, H)).astype(np.float32)).to(torch.bfloat16)
+    # expert e's weights have magnitude 0.02 * (1 + e): scales and globals differ by expert
+    mag = torch.tensor([0.02 * (1 + e) for e in range(E)]).view(E, 1, 1)
+    w13 = (torch.from_numpy(rng.standard_normal((E, 2 * I, H)).astype(np.float32)) * mag).to(torch.bfloat16)
+    w2 = (torch.from_numpy(rng.standard_normal((E, H, I)).astype(np.float32)) * mag).to(torch.bfloat16)
+    rows = np.arange(18)
+    globs = {}
+    if fmt == 0:
+        ya, ys, a13, s13, a2, s2 = _bits(y_bf), None, _bits(w13), None, _bits(w2), None
+        y_d = y_bf.double()
+        w13_d = [w13[e].double() for e in range(E)]
+        w2_d = [w2[e].double() for e in range(E)]
+    elif fmt == 1:
+        ya, ys = oracle.quantize_fp8_rows(_bits(y_bf))
+        a13, s13 = oracle.quantize_fp8_weight(_bits(w13))
+        a2, s2 = oracle.quantize_fp8_weight(_bits(w2))
+        assert len({float(s13[e].max()) for e in range(E)}) == E
+
+        def deq(q, s, bs):
+            v = torch.from_numpy(np.ascontiguousarray(q)).view(torch.float8_e4m3fn).double()
+            return v * torch.from_numpy(np.kron(s, np.ones(bs))).double()
+
+        y_d = deq(ya, ys, (1, 128))
+        w13_d = [deq(a13[e], s13[e], (128, 128)) for e in range(E)]
+        w2_d = [deq(a2[e], s2[e], (128, 128)) for e in range(E)]
+    else:
+        g1 = float(np.float32(np.abs(y_bf.float().numpy()).max() / 2688.0))
+        ya, ys = oracle.quantize_nvfp4_rows(_bits(y_bf), g1)
+        a13, s13, g13 = _nvfp4_per_expert(oracle, w13)
+        a2, s2, g2w = _nvfp4_per_expert(oracle, w2)
+        assert len(set(g13.tolist())) == E
+        globs = dict(w13_global=g13, w2_global=g2w, fc1_in_global=g1, fc2_in_global=0.004)
+
+        def deq(packed, sc, glob):
+            R, half = packed.shape
+            codes = np.stack([packed & 0xF, packed >> 4], -1).reshape(R, half * 2)
+            v = torch.from_numpy(np.ascontiguousarray(codes)).to(torch.uint8)
+            # E2M1 magnitudes from the format's definition: 0, .5, 1, 1.5, 2, 3, 4, 6; bit 3 the sign
+            mags = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float64)
+            val = mags[(v & 7).long()] * torch.where((v & 8) != 0, -1.0, 1.0).double()
+            scl = torch.from_numpy(np.ascontiguousarray(sc)).view(torch.float8_e4m3fn).double()
+            return val * scl.repeat_interleave(16, dim=1) * float(glob)
+
+        y_d = deq(ya, ys, g1)
+        w13_d = [deq(a13[e], s13[e], g13[e]) for e in range(E)]
+        w2_d = [deq(a2[e], s2[e], g2w[e]) for e in range(E)]
+    out, act = oracle.grouped_mlp_rows(fmt, ya, ys, H, I, E, offsets, a13, s13, a2, s2, rows, want_act=True,
+                                       **globs)
+    got = oracle.bf16_to_f64(out)
+    for e in range(E):
+        r = np.arange(offsets[e], offsets[e + 1])
+        if len(r) == 0:
+            continue
+        a = _torch_ffn(y_d[r], w13_d[e], None, I).numpy()
+        if fmt == 0:
+            want_act = oracle.bf16_to_f64(oracle.f64_to_bf16(a))
+            assert np.all(np.abs(act[r] - want_act) <= np.abs(want_act) * 2.0 ** -7 + 1e-12), e
+        else:
+            want_act = _e4m3_round_trip_blocks(a.astype(np.float32), None if fmt == 1 else 16,
+                                               None if fmt == 1 else globs["fc2_in_global"])
+            # a code may differ only where the fp32 product lies at a rounding boundary
+            assert np.mean(np.abs(act[r] - want_act) <= np.abs(want_act) * 2.0 ** -3 + 1e-9) > 0.99, e
+        ref = act[r] @ w2_d[e].numpy().T
+        assert np.all(np.abs(got[r] - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-12), e
+        # and the expert's own weights matter: another expert's FC2 gives a different result
+        other = act[r] @ w2_d[(e + 1) % E].numpy().T
+        assert np.abs(got[r] - other).max() > 10 * np.abs(ref).max() * 2.0 ** -8
