@@ -312,7 +312,8 @@ MOE_API moe_status moe_grouped_mlp_kernel_count(const moe_shape* shape, const mo
  * stream -- before FC1, between FC1 and FC2, and after FC2 -- and then forgets
  * them.  Where one kernel runs both GEMMs (moe_grouped_mlp_kernel_count 1),
  * the between and after events are both recorded after it.  Pass NULLs to
- * cancel.  Used to time the two GEMM kernels separately
+ * cancel.  Under stream capture the records become event-record nodes of the
+ * graph (cudaEventRecordExternal), so every replay records them again.  Used to time the two GEMM kernels separately
  * inside a step (TensorRT-LLM PR #16190 "Update CuTeDSL MegaMoE kernels",
  * commit list: the microbench reports kernel-level times). */
 MOE_API moe_status moe_profile_next_grouped_mlp(void* ev_before_fc1, void* ev_after_fc1, void* ev_after_fc2);

@@ -546,12 +546,12 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
   if (grid < 1) grid = 1;
 
   const ProfileEvents prof = take_profile_events();
-  if (prof.before_fc1 && (e = cudaEventRecord(prof.before_fc1, st)) != cudaSuccess) return e;
+  if (prof.before_fc1 && (e = record_profile_event(prof.before_fc1, st)) != cudaSuccess) return e;
   grouped_mlp_bf16_kernel<<<(unsigned)grid, kThreads, kDynSmem, st>>>(ty, tw13, tact, tw2, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // one kernel runs both GEMMs: the FC1/FC2 boundary event is recorded with the end
-  if (prof.after_fc1 && (e = cudaEventRecord(prof.after_fc1, st)) != cudaSuccess) return e;
-  if (prof.after_fc2 && (e = cudaEventRecord(prof.after_fc2, st)) != cudaSuccess) return e;
+  if (prof.after_fc1 && (e = record_profile_event(prof.after_fc1, st)) != cudaSuccess) return e;
+  if (prof.after_fc2 && (e = record_profile_event(prof.after_fc2, st)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

@@ -365,7 +365,7 @@ cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shap
     return e;
   const int64_t m_tiles_bound = (l.capacity + 2 * BMC - 1) / (2 * BMC) + s.E;
   const ProfileEvents prof = take_profile_events();
-  if (prof.before_fc1 && (e = cudaEventRecord(prof.before_fc1, st)) != cudaSuccess) return e;
+  if (prof.before_fc1 && (e = record_profile_event(prof.before_fc1, st)) != cudaSuccess) return e;
 
   PairParams p1;
   p1.offsets = h.padded_offsets;
@@ -381,7 +381,7 @@ cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shap
   p1.nt = (int)(s.I / 128);
   p1.nkb = (int)(s.H / BK);
   if ((e = launch_pair<kFc1SwiGLU>(ta1, tb1, p1, m_tiles_bound * p1.nt, st)) != cudaSuccess) return e;
-  if (prof.after_fc1 && (e = cudaEventRecord(prof.after_fc1, st)) != cudaSuccess) return e;
+  if (prof.after_fc1 && (e = record_profile_event(prof.after_fc1, st)) != cudaSuccess) return e;
 
   PairParams p2 = p1;
   p2.out = static_cast<uint8_t*>(out_fc2);
@@ -393,7 +393,7 @@ cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shap
   p2.nt = (int)((s.H + BN - 1) / BN);
   p2.nkb = (int)(s.I / BK);
   if ((e = launch_pair<kFc2>(ta2, tb2, p2, m_tiles_bound * p2.nt, st)) != cudaSuccess) return e;
-  if (prof.after_fc2 && (e = cudaEventRecord(prof.after_fc2, st)) != cudaSuccess) return e;
+  if (prof.after_fc2 && (e = record_profile_event(prof.after_fc2, st)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

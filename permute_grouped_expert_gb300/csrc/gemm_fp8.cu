@@ -468,7 +468,7 @@ cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, 
     return e;
   const int64_t m_tiles_bound = (l.capacity + BM - 1) / BM + s.E;
   const ProfileEvents prof = take_profile_events();
-  if (prof.before_fc1 && (e = cudaEventRecord(prof.before_fc1, st)) != cudaSuccess) return e;
+  if (prof.before_fc1 && (e = record_profile_event(prof.before_fc1, st)) != cudaSuccess) return e;
 
   Fp8Params p1;
   p1.offsets = h.padded_offsets;
@@ -487,7 +487,7 @@ cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, 
   p1.nkb = (int)(s.H / BK);
   p1.n_blocks_b = (int)(2 * s.I / 128);
   if ((e = launch_one<kFc1SwiGLU>(ta1, tb1, p1, m_tiles_bound * p1.nt, st)) != cudaSuccess) return e;
-  if (prof.after_fc1 && (e = cudaEventRecord(prof.after_fc1, st)) != cudaSuccess) return e;
+  if (prof.after_fc1 && (e = record_profile_event(prof.after_fc1, st)) != cudaSuccess) return e;
 
   Fp8Params p2 = p1;
   p2.a_scales = act_scales;
@@ -502,7 +502,7 @@ cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, 
   p2.nkb = (int)(s.I / BK);
   p2.n_blocks_b = (int)(s.H / 128);
   if ((e = launch_one<kFc2>(ta2, tb2, p2, m_tiles_bound * p2.nt, st)) != cudaSuccess) return e;
-  if (prof.after_fc2 && (e = cudaEventRecord(prof.after_fc2, st)) != cudaSuccess) return e;
+  if (prof.after_fc2 && (e = record_profile_event(prof.after_fc2, st)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

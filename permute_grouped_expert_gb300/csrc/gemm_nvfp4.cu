@@ -519,7 +519,7 @@ cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s
   if ((e = make_tensor_map_2d(&x2s, act_scales, U8, 1, cap, s.I / 16, BNT, BKR / 16, NO)) != cudaSuccess) return e;
   const int64_t n_tiles_bound = (l.capacity + BNT - 1) / BNT + s.E;
   const ProfileEvents prof = take_profile_events();
-  if (prof.before_fc1 && (e = cudaEventRecord(prof.before_fc1, st)) != cudaSuccess) return e;
+  if (prof.before_fc1 && (e = record_profile_event(prof.before_fc1, st)) != cudaSuccess) return e;
 
   Fp4Params p1;
   p1.offsets = h.padded_offsets;
@@ -537,7 +537,7 @@ cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s
   p1.nmt = (int)(s.I / 64);
   p1.nkr = (int)(s.H / BKR);
   if ((e = launch_one<kFc1SwiGLU>(w1, w1s, x1, x1s, p1, n_tiles_bound * p1.nmt, st)) != cudaSuccess) return e;
-  if (prof.after_fc1 && (e = cudaEventRecord(prof.after_fc1, st)) != cudaSuccess) return e;
+  if (prof.after_fc1 && (e = record_profile_event(prof.after_fc1, st)) != cudaSuccess) return e;
 
   Fp4Params p2 = p1;
   p2.out = static_cast<uint8_t*>(out_fc2);
@@ -551,7 +551,7 @@ cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s
   p2.nmt = (int)(s.H / BMW);
   p2.nkr = (int)(s.I / BKR);
   if ((e = launch_one<kFc2>(w2m, w2s, x2, x2s, p2, n_tiles_bound * p2.nmt, st)) != cudaSuccess) return e;
-  if (prof.after_fc2 && (e = cudaEventRecord(prof.after_fc2, st)) != cudaSuccess) return e;
+  if (prof.after_fc2 && (e = record_profile_event(prof.after_fc2, st)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

@@ -86,6 +86,10 @@ ProfileEvents take_profile_events() {
 
 void set_profile_events(const ProfileEvents& ev) { g_profile = ev; }
 
+cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t st) {
+  return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+}
+
 thread_local int64_t g_debug_mlp_silent = -1;
 
 int64_t take_debug_mlp_silent_tile() {

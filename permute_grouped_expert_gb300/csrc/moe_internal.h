@@ -111,6 +111,9 @@ struct ProfileEvents {
   cudaEvent_t before_fc1 = nullptr, after_fc1 = nullptr, after_fc2 = nullptr;
 };
 ProfileEvents take_profile_events();
+// Records a profiling event on `st`; under stream capture the record becomes an
+// event-record node of the graph (recorded again on every replay).
+cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t st);
 // Testing hook (moe_debug_next_grouped_mlp_silent_token_tile); consumed and
 // cleared by the next fused bf16 grouped-MLP launch of this host thread.
 int64_t take_debug_mlp_silent_tile();
