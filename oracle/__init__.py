@@ -244,6 +244,43 @@ def combine(o_bf16: np.ndarray, row_of: np.ndarray, perm_probs=None) -> np.ndarr
     return y
 
 
+def combine_backward(g_y: np.ndarray, pre: dict, cap: int, o=None, perm_probs=None):
+    """Backward of combine: (gO bf16 [cap, H], gw fp32 [cap] or None).  gw is
+    formed when both ``o`` and ``perm_probs`` are given.  Rows at or beyond
+    ``pre['valid_rows']`` are zeros here and carry no meaning."""
+    gy = _c(g_y, np.uint16)
+    T, H = gy.shape
+    ro = np.ascontiguousarray(pre["row_of"], dtype=np.int32)
+    K = ro.shape[1]
+    E = len(pre["counts"])
+    ov = _c(o, np.uint16) if o is not None else None
+    pp = _c(perm_probs, np.float32)
+    g_o = np.zeros((max(cap, 1), H), np.uint16)
+    g_w = np.zeros(max(cap, 1), np.float32) if (o is not None and perm_probs is not None) else None
+    _load().moe_oracle_combine_backward(
+        _p(gy), ctypes.c_int64(T), ctypes.c_int64(H), ctypes.c_int64(E), ctypes.c_int64(K), _p(ro),
+        _p(pre["counts"]), _p(pre["offsets"]), ctypes.c_int64(cap), _p(ov), _p(pp), _p(g_o), _p(g_w))
+    return g_o[:cap], (g_w[:cap] if g_w is not None else None)
+
+
+def dispatch_backward(fmt: int, routing_map, row_of, E: int, g_y, g_yp=None):
+    """Backward of dispatch: (gx bf16 [T, H], gp fp32 in the routing layout or None)."""
+    rmap = _c(routing_map, np.int16 if fmt == ROUTING_DENSE else np.uint8)
+    ro = np.ascontiguousarray(row_of, dtype=np.int32)
+    T, K = ro.shape
+    gy = _c(g_y, np.uint16)
+    H = gy.shape[1]
+    gyp = _c(g_yp, np.float32)
+    g_x = np.empty((T, H), np.uint16)
+    g_p = None
+    if g_yp is not None:
+        g_p = np.empty((T, K) if fmt == ROUTING_DENSE else (T, E), np.float32)
+    _load().moe_oracle_dispatch_backward(
+        ctypes.c_int(fmt), _p(rmap), ctypes.c_int64(T), ctypes.c_int64(E), ctypes.c_int64(K), ctypes.c_int64(H),
+        _p(ro), _p(gy), _p(gyp), _p(g_x), _p(g_p))
+    return g_x, g_p
+
+
 def layer_per_token(fmt: int, routing_fmt: int, routing_map, probs, E: int, K: int, x, x_scales, H: int,
                     I: int, w13, w13_scales, w2, w2_scales, tokens, w13_global=None, w2_global=None,
                     fc1_in_global: float = 0.0, fc2_in_global: float = 0.0) -> np.ndarray:

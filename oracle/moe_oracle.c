@@ -108,6 +108,17 @@ ORACLE_API double moe_oracle_e4m3_to_f64(uint8_t c) {
   return neg ? -v : v;
 }
 
+/* Decoded values of every E4M3 code and every E2M1 code, filled once when the
+ * library loads from the decoders above and below (a cache of their results:
+ * the searches and operand reads use the same values they would compute). */
+ORACLE_API double moe_oracle_e2m1_to_f64(uint8_t c);
+static double g_e4m3_value[256];
+static double g_e2m1_value[16];
+__attribute__((constructor)) static void oracle_fill_code_tables(void) {
+  for (int c = 0; c < 256; c++) g_e4m3_value[c] = moe_oracle_e4m3_to_f64((uint8_t)c);
+  for (int c = 0; c < 16; c++) g_e2m1_value[c] = moe_oracle_e2m1_to_f64((uint8_t)c);
+}
+
 /* Encode a binary32 into E4M3 by rounding to the nearest finite code (ties to the
  * code with an even fraction field, i.e. the even code), saturating magnitudes
  * beyond 448 to 448.  The search runs over the code table, so no library
@@ -121,14 +132,14 @@ ORACLE_API uint8_t moe_oracle_f32_to_e4m3(float v) {
   int lo = 0, hi = 0x7E;
   while (lo < hi) {
     int mid = (lo + hi + 1) / 2;
-    if (moe_oracle_e4m3_to_f64((uint8_t)mid) <= a)
+    if (g_e4m3_value[mid] <= a)
       lo = mid;
     else
       hi = mid - 1;
   }
   int c = lo;
-  double below = moe_oracle_e4m3_to_f64((uint8_t)c);
-  double above = moe_oracle_e4m3_to_f64((uint8_t)(c + 1));
+  double below = g_e4m3_value[c];
+  double above = g_e4m3_value[c + 1];
   double d_lo = a - below, d_hi = above - a;
   int pick;
   if (d_lo < d_hi)
@@ -370,24 +381,30 @@ ORACLE_API void moe_oracle_quantize_fp8_rows(const uint16_t* x, int64_t T, int64
  * (one fp32 scale per 128x128 block). */
 ORACLE_API void moe_oracle_quantize_fp8_weight(const uint16_t* w, int64_t G, int64_t N, int64_t Kd,
                                                uint8_t* q, float* scales) {
-  float* blk = (float*)malloc(sizeof(float) * 128 * 128);
-  uint8_t* qb = (uint8_t*)malloc(128 * 128);
-  for (int64_t g = 0; g < G; g++)
-    for (int64_t nb = 0; nb < N / 128; nb++)
-      for (int64_t kb = 0; kb < Kd / 128; kb++) {
-        for (int64_t i = 0; i < 128; i++)
-          for (int64_t j = 0; j < 128; j++)
-            blk[i * 128 + j] =
-                (float)moe_oracle_bf16_to_f64(w[(g * N + nb * 128 + i) * Kd + kb * 128 + j]);
-        float s;
-        quant_block_e4m3(blk, 128 * 128, 1, qb, 1, &s);
-        for (int64_t i = 0; i < 128; i++)
-          for (int64_t j = 0; j < 128; j++)
-            q[(g * N + nb * 128 + i) * Kd + kb * 128 + j] = qb[i * 128 + j];
-        scales[(g * (N / 128) + nb) * (Kd / 128) + kb] = s;
-      }
-  free(blk);
-  free(qb);
+  /* every 128x128 block is quantized on its own, so blocks run in parallel */
+  const int64_t nblk = G * (N / 128) * (Kd / 128);
+#pragma omp parallel
+  {
+    float* blk = (float*)malloc(sizeof(float) * 128 * 128);
+    uint8_t* qb = (uint8_t*)malloc(128 * 128);
+#pragma omp for schedule(static)
+    for (int64_t id = 0; id < nblk; id++) {
+      const int64_t g = id / ((N / 128) * (Kd / 128));
+      const int64_t nb = (id / (Kd / 128)) % (N / 128);
+      const int64_t kb = id % (Kd / 128);
+      for (int64_t i = 0; i < 128; i++)
+        for (int64_t j = 0; j < 128; j++)
+          blk[i * 128 + j] = (float)moe_oracle_bf16_to_f64(w[(g * N + nb * 128 + i) * Kd + kb * 128 + j]);
+      float s;
+      quant_block_e4m3(blk, 128 * 128, 1, qb, 1, &s);
+      for (int64_t i = 0; i < 128; i++)
+        for (int64_t j = 0; j < 128; j++)
+          q[(g * N + nb * 128 + i) * Kd + kb * 128 + j] = qb[i * 128 + j];
+      scales[(g * (N / 128) + nb) * (Kd / 128) + kb] = s;
+    }
+    free(blk);
+    free(qb);
+  }
 }
 
 /* ------------------------------------------------------------------------- */
@@ -431,20 +448,24 @@ static void quant_rows_nvfp4_f32(const float* v, int64_t R, int64_t Kd, float gl
 /* bf16 rows [R][Kd] -> NVFP4 with the given global scale. */
 ORACLE_API void moe_oracle_quantize_nvfp4_rows(const uint16_t* x, int64_t R, int64_t Kd,
                                                float global, uint8_t* packed, uint8_t* scales) {
-  float* row = (float*)malloc(sizeof(float) * (size_t)Kd);
-  for (int64_t r = 0; r < R; r++) {
-    for (int64_t i = 0; i < Kd; i++) row[i] = (float)moe_oracle_bf16_to_f64(x[r * Kd + i]);
-    quant_rows_nvfp4_f32(row, 1, Kd, global, packed + r * (Kd / 2), scales + r * (Kd / 16));
+  /* rows are independent, so they run in parallel */
+#pragma omp parallel
+  {
+    float* row = (float*)malloc(sizeof(float) * (size_t)Kd);
+#pragma omp for schedule(static)
+    for (int64_t r = 0; r < R; r++) {
+      for (int64_t i = 0; i < Kd; i++) row[i] = (float)moe_oracle_bf16_to_f64(x[r * Kd + i]);
+      quant_rows_nvfp4_f32(row, 1, Kd, global, packed + r * (Kd / 2), scales + r * (Kd / 16));
+    }
+    free(row);
   }
-  free(row);
 }
 
 static double nvfp4_value(const uint8_t* packed, const uint8_t* scales, int64_t Kd, int64_t r,
                           int64_t i, double global) {
   uint8_t byte = packed[r * (Kd / 2) + i / 2];
   uint8_t code = (i % 2 == 0) ? (byte & 0xF) : (byte >> 4);
-  return moe_oracle_e2m1_to_f64(code) * moe_oracle_e4m3_to_f64(scales[r * (Kd / 16) + i / 16]) *
-         global;
+  return g_e2m1_value[code] * g_e4m3_value[scales[r * (Kd / 16) + i / 16]] * global;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -473,7 +494,7 @@ typedef struct {
 static double act_value(const operand* a, int64_t Kd, int64_t r, int64_t i) {
   if (a->fmt == 0) return moe_oracle_bf16_to_f64(((const uint16_t*)a->data)[r * Kd + i]);
   if (a->fmt == 1)
-    return moe_oracle_e4m3_to_f64(((const uint8_t*)a->data)[r * Kd + i]) *
+    return g_e4m3_value[((const uint8_t*)a->data)[r * Kd + i]] *
            (double)((const float*)a->scales)[r * (Kd / 128) + i / 128];
   return nvfp4_value((const uint8_t*)a->data, (const uint8_t*)a->scales, Kd, r, i, a->global);
 }
@@ -485,7 +506,7 @@ static double weight_value(const operand* w, const float* globals, int64_t N, in
   int64_t row = e * N + n;
   if (w->fmt == 0) return moe_oracle_bf16_to_f64(((const uint16_t*)w->data)[row * Kd + i]);
   if (w->fmt == 1)
-    return moe_oracle_e4m3_to_f64(((const uint8_t*)w->data)[row * Kd + i]) *
+    return g_e4m3_value[((const uint8_t*)w->data)[row * Kd + i]] *
            (double)((const float*)w->scales)[(e * (N / 128) + n / 128) * (Kd / 128) + i / 128];
   return nvfp4_value((const uint8_t*)w->data, (const uint8_t*)w->scales, Kd, row, i,
                      (double)globals[e]);
@@ -601,6 +622,86 @@ ORACLE_API void moe_oracle_combine(const uint16_t* o, int64_t H, const int32_t* 
       }
       y[t * H + h] = moe_oracle_f64_to_bf16(acc);
     }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Backward of combine and of dispatch                                         */
+/* ------------------------------------------------------------------------- */
+
+/* [ALLGATHER], Testing / Output and gradient regression: hidden-state and
+ * probability gradients for the backward of the combine; [SYNC-FREE], What does
+ * this PR do?: the combine's backward is a dispatch sized by the same host
+ * capacity.  The combine computed y[t] = sum_k w(r) * O[r] over the kept rows
+ * r = row_of[t][k], so for an output gradient gy:
+ *   gO[r] = bf16( w(r) * gy[t] )            (a dispatch of gy, scaled per row)
+ *   gw[r] = sum_h gy[t][h] * O[r][h]        (stored as fp32)
+ * with w(r) = perm_probs[r], or 1 when perm_probs is NULL (gw then not formed).
+ * Pad rows [offsets[e] + counts[e], offsets[e+1]) below cap get gO = 0 and
+ * gw = 0; rows at or beyond min(offsets[E], cap) are not written.
+ * o may be NULL when gw is not wanted (gw NULL). */
+ORACLE_API void moe_oracle_combine_backward(const uint16_t* gy, int64_t T, int64_t H, int64_t E, int64_t K,
+                                            const int32_t* row_of, const int32_t* counts,
+                                            const int32_t* offsets, int64_t cap, const uint16_t* o,
+                                            const float* perm_probs, uint16_t* g_o, float* g_w) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; t++)
+    for (int64_t k = 0; k < K; k++) {
+      int32_t r = row_of[t * K + k];
+      if (r < 0) continue;
+      double w = perm_probs ? (double)perm_probs[r] : 1.0;
+      double dot = 0.0;
+      for (int64_t h = 0; h < H; h++) {
+        double g = moe_oracle_bf16_to_f64(gy[t * H + h]);
+        g_o[(int64_t)r * H + h] = moe_oracle_f64_to_bf16(w * g);
+        if (o) dot += g * moe_oracle_bf16_to_f64(o[(int64_t)r * H + h]);
+      }
+      if (g_w) g_w[r] = f64_to_f32(dot);
+    }
+  for (int64_t e = 0; e < E; e++)
+    for (int64_t r = (int64_t)offsets[e] + counts[e]; r < offsets[e + 1] && r < cap; r++) {
+      for (int64_t h = 0; h < H; h++) g_o[r * H + h] = 0;
+      if (g_w) g_w[r] = 0.0f;
+    }
+}
+
+/* The dispatch computed Y[r] = x[t] and Yp[r] = p(t,k) for every kept route
+ * (t,k) -> r, so for row gradients gY and probability gradients gYp:
+ *   gx[t] = bf16( sum over k ascending of gY[row_of[t][k]] )   (a combine with
+ *           weight 1; tokens whose routes were all dropped get zeros)
+ *   gp(t,k) = gYp[row_of[t][k]], 0 for a dropped route or an empty slot,
+ * written in the routing layout: dense [T][K]; sparse [T][E] (the entry of the
+ * slot's expert; every other entry 0).  gYp and gp may be NULL together. */
+ORACLE_API int moe_oracle_dispatch_backward(int format, const void* map, int64_t T, int64_t E, int64_t K,
+                                            int64_t H, const int32_t* row_of, const uint16_t* g_y,
+                                            const float* g_yp, uint16_t* g_x, float* g_p) {
+  int32_t* route = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T * K + 1));
+  int status = build_routes(format, map, T, E, K, route);
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; t++) {
+    for (int64_t h = 0; h < H; h++) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; k++) {
+        int32_t r = row_of[t * K + k];
+        if (r >= 0) acc += moe_oracle_bf16_to_f64(g_y[(int64_t)r * H + h]);
+      }
+      g_x[t * H + h] = moe_oracle_f64_to_bf16(acc);
+    }
+    if (!g_p) continue;
+    if (format == 0) {
+      for (int64_t k = 0; k < K; k++) {
+        int32_t r = row_of[t * K + k];
+        g_p[t * K + k] = (r >= 0) ? g_yp[r] : 0.0f;
+      }
+    } else {
+      for (int64_t e = 0; e < E; e++) g_p[t * E + e] = 0.0f;
+      for (int64_t k = 0; k < K; k++) {
+        int32_t r = row_of[t * K + k];
+        if (r >= 0 && route[t * K + k] >= 0) g_p[t * E + route[t * K + k]] = g_yp[r];
+      }
+    }
+  }
+  free(route);
+  return status;
 }
 
 /* ------------------------------------------------------------------------- */

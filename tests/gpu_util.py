@@ -107,3 +107,56 @@ def gather_rows(o_full, row_of, perm_probs):
 def mismatch_fraction(got: np.ndarray, ref: np.ndarray) -> float:
     """Fraction of elements that are not bit-identical."""
     return float(np.mean(np.asarray(got) != np.asarray(ref))) if np.asarray(ref).size else 0.0
+
+
+def expert_of_rows(offsets, rows):
+    """Expert owning each permuted row (offsets[e] <= row < offsets[e+1])."""
+    return np.searchsorted(np.asarray(offsets), np.asarray(rows), side="right") - 1
+
+
+def segment_edge_rows(pre, cap):
+    """First and last valid (routed) row of every non-empty expert segment below the capacity."""
+    off, cnt = pre["offsets"], pre["counts"]
+    rows = []
+    for e in range(len(cnt)):
+        if cnt[e] == 0 or off[e] >= cap:
+            continue
+        last = min(off[e] + cnt[e], cap) - 1
+        rows += [off[e], last]
+    return np.unique(np.array(rows, np.int64))
+
+
+def largest_expert_rows(pre, cap, n):
+    """n rows spread evenly over the largest expert's valid rows (all its token tiles)."""
+    e = int(np.argmax(pre["counts"]))
+    beg, end = int(pre["offsets"][e]), int(min(pre["offsets"][e] + pre["counts"][e], cap))
+    return np.unique(np.linspace(beg, end - 1, n).astype(np.int64)), e
+
+
+def oracle_rows_chunked(oracle, fmt, yq, ys, pre, rows, H, I, expert_weights, chunk=16, **globs):
+    """Oracle FFN of the given permuted rows, a chunk of experts at a time so
+    that only that chunk's oracle-format weights are in host memory.
+    expert_weights(experts) -> (w13, w13_scales, w2, w2_scales, g13, g2) for
+    those experts in the oracle's format (g13 / g2 None except NVFP4).
+    Returns (rows in evaluation order, bf16 outputs [n, H])."""
+    rows = np.unique(np.asarray(rows, np.int64))
+    owner = expert_of_rows(pre["offsets"], rows)
+    experts = sorted(set(owner.tolist()))
+    sel_all, out_all = [], []
+    for i in range(0, len(experts), chunk):
+        ex = experts[i:i + chunk]
+        q13, s13, q2, s2, g13, g2 = expert_weights(ex)
+        sel, off = [], [0]
+        for e in ex:
+            rr = rows[owner == e]
+            sel.append(rr)
+            off.append(off[-1] + len(rr))
+        sel = np.concatenate(sel)
+        extra = dict(globs)
+        if g13 is not None:
+            extra.update(w13_global=g13, w2_global=g2)
+        ob, _ = oracle.grouped_mlp_rows(fmt, yq[sel], None if ys is None else ys[sel], H, I, len(ex),
+                                        np.array(off, np.int32), q13, s13, q2, s2, np.arange(len(sel)), **extra)
+        sel_all.append(sel)
+        out_all.append(ob)
+    return np.concatenate(sel_all), np.concatenate(out_all)

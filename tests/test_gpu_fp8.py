@@ -97,16 +97,40 @@ def test_fp8_layer_all_rows(oracle, moe, name, w):
 
 def test_dsv3_layer_full_size_sampled(oracle, moe):
     """8192 tokens, hidden 7168, 256 Zipf(1.2)-skewed experts, top-8,
-    intermediate 2048, FP8: the oracle recomputes the rows of 6 sampled tokens."""
+    intermediate 2048, FP8, in the launch configuration the benchmark times.
+    The oracle recomputes: every route of 6 sampled tokens (and their combined
+    outputs); the first and the last valid row of every expert segment (the
+    first token tile and the ragged last tile of all 256 experts, across every
+    CTA's share of the tile list); 128 rows spread over the largest expert
+    (thousands of rows, dozens of token tiles)."""
+    from gpu_util import largest_expert_rows, oracle_rows_chunked, segment_edge_rows
+
     w = workloads.WORKLOADS["dsv3"]
     r = run_layer_fp8(moe, w, seed=0)
     pre = oracle.preprocess(r["fmt"], r["rmap"], w.T, w.E, w.K, w.m, r["cap"])
     assert pre["counts"].max() > 10 * np.median(pre["counts"])
     toks = np.sort(np.random.default_rng(3).choice(w.T, 6, replace=False))
-    rows = np.unique(pre["row_of"][toks][pre["row_of"][toks] >= 0])
-    sel, ob = _oracle_rows(oracle, w, r, rows, pre)
+    tok_rows = np.unique(pre["row_of"][toks][pre["row_of"][toks] >= 0])
+    head_rows, head = largest_expert_rows(pre, r["cap"], 128)
+    assert pre["counts"][head] > 60 * 128  # the Zipf head spans dozens of token tiles
+    edge_rows = segment_edge_rows(pre, r["cap"])
+    assert len(edge_rows) >= 2 * 250
+    rows = np.unique(np.concatenate([tok_rows, head_rows, edge_rows]))
+
+    xq, xs = oracle.quantize_fp8_rows(workloads.bf16_bits(r["x"]))
+    yq, _ = oracle.dispatch(r["fmt"], r["rmap"], None, pre, xq, r["cap"], w.E, w.K)
+    ys, _ = oracle.dispatch(r["fmt"], r["rmap"], None, pre, xs, r["cap"], w.E, w.K)
+
+    def weights(ex):
+        q13, s13 = oracle.quantize_fp8_weight(workloads.bf16_bits(r["w13"][ex]))
+        q2, s2 = oracle.quantize_fp8_weight(workloads.bf16_bits(r["w2"][ex]))
+        return q13, s13, q2, s2, None, None
+
+    sel, ob = oracle_rows_chunked(oracle, 1, yq, ys, pre, rows, w.H, w.I, weights)
     got = bits(r["o"][torch.from_numpy(sel).cuda()])
-    assert rel_err(oracle.bf16_to_f64(got), oracle.bf16_to_f64(ob)) <= TOL_FP8
+    for name, subset in (("edges", edge_rows), ("largest expert", head_rows), ("sampled tokens", tok_rows)):
+        m = np.isin(sel, subset)
+        assert rel_err(oracle.bf16_to_f64(got[m]), oracle.bf16_to_f64(ob[m])) <= TOL_FP8, name
     _, po = oracle.dispatch(r["fmt"], r["rmap"], r["probs"], pre, np.zeros((w.T, 1), np.uint8), r["cap"], w.E, w.K)
     o_full = np.zeros((r["cap"], w.H), np.uint16)
     o_full[sel] = ob

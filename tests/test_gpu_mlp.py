@@ -76,12 +76,17 @@ def test_grouped_mlp_bf16_all_rows(oracle, moe, name, w):
     assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(ref), o_rows, wts) <= TOL_BF16
 
 
-def _sampled_check(oracle, w, r, n_tokens=48, seed=0):
-    """Oracle on a sample of tokens (all their routes) at full size."""
+def _sampled_check(oracle, w, r, n_tokens=48, seed=0, edges=False):
+    """Oracle on a sample of tokens (all their routes) at full size; with
+    edges, also the first and last valid row of every expert segment."""
+    from gpu_util import segment_edge_rows
+
     pre = oracle.preprocess(r["fmt"], r["rmap"], w.T, w.E, w.K, w.m, r["cap"])
     rng = np.random.default_rng(seed)
     toks = np.sort(rng.choice(w.T, n_tokens, replace=False))
     rows = np.unique(pre["row_of"][toks][pre["row_of"][toks] >= 0])
+    if edges:
+        rows = np.unique(np.concatenate([rows, segment_edge_rows(pre, r["cap"])]))
     xb = workloads.bf16_bits(r["x"])
     yo, po = oracle.dispatch(r["fmt"], r["rmap"], r["probs"], pre, xb, r["cap"], w.E, w.K)
     experts = sorted({int(np.searchsorted(pre["offsets"], rr, side="right") - 1) for rr in rows})
@@ -118,7 +123,7 @@ def test_mid_layer_full_size_sampled(oracle, moe):
     cap = oracle.capacity(rows, w.cap_factor)
     r = run_layer_bf16(moe, w, seed=31, cap=cap)
     assert handle_np(r["handle"], w.T, w.K, cap)["overflow"] == 0
-    _sampled_check(oracle, w, r)
+    _sampled_check(oracle, w, r, edges=True)
 
 
 def test_skewed_experts_with_empty_ones(oracle, moe):

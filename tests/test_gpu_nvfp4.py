@@ -119,11 +119,41 @@ def test_nvfp4_layer_all_tokens(oracle, moe, name, w):
             assert not o_all[row].any()
 
 
-@pytest.mark.parametrize("name", ["decode64", "decode256"])
-def test_decode_full_size_sampled(oracle, moe, name):
-    """64 / 256 tokens, hidden 7168, 256 experts, top-8, intermediate 2048, NVFP4:
-    the oracle recomputes every route of 4 sampled tokens."""
+@pytest.mark.parametrize("name,n_tokens", [("decode64", 64), ("decode256", 32)])
+def test_decode_full_size(oracle, moe, name, n_tokens):
+    """64 / 256 tokens, hidden 7168, 256 experts, top-8, intermediate 2048,
+    NVFP4, in the launch configuration the benchmark times: the oracle
+    recomputes every route of every token (decode64) or of 32 sampled tokens
+    (decode256), and their combined outputs."""
+    from gpu_util import oracle_rows_chunked
+
     w = workloads.WORKLOADS[name]
     r = run_layer_nvfp4(moe, w, seed=0)
-    toks = np.sort(np.random.default_rng(5).choice(w.T, 4, replace=False))
-    _check(oracle, w, r, toks)
+    toks = np.arange(w.T) if n_tokens >= w.T else np.sort(
+        np.random.default_rng(5).choice(w.T, n_tokens, replace=False))
+    pre = oracle.preprocess(r["fmt"], r["rmap"], w.T, w.E, w.K, w.m, r["cap"])
+    rows = pre["row_of"][toks]
+    rows = np.unique(rows[rows >= 0])
+    xq, xs = oracle.quantize_nvfp4_rows(workloads.bf16_bits(r["x"]), float(r["gx"]))
+    yq, _ = oracle.dispatch(r["fmt"], r["rmap"], None, pre, xq, r["cap"], w.E, w.K)
+    ys, _ = oracle.dispatch(r["fmt"], r["rmap"], None, pre, xs, r["cap"], w.E, w.K)
+
+    def weights(ex):
+        q13, s13, q2, s2 = [], [], [], []
+        for e in ex:
+            a, b = oracle.quantize_nvfp4_rows(workloads.bf16_bits(r["w13"][e]), float(r["g13"][e]))
+            c, d = oracle.quantize_nvfp4_rows(workloads.bf16_bits(r["w2"][e]), float(r["g2"][e]))
+            q13.append(a), s13.append(b), q2.append(c), s2.append(d)
+        return np.stack(q13), np.stack(s13), np.stack(q2), np.stack(s2), r["g13"][ex], r["g2"][ex]
+
+    sel, ob = oracle_rows_chunked(oracle, 2, yq, ys, pre, rows, w.H, w.I, weights,
+                                  fc1_in_global=float(r["gx"]), fc2_in_global=float(np.float32(FC2_IN_GLOBAL)))
+    got = bits(r["o"][torch.from_numpy(sel).cuda()])
+    assert rel_err(oracle.bf16_to_f64(got), oracle.bf16_to_f64(ob)) <= TOL_FP4
+    _, po = oracle.dispatch(r["fmt"], r["rmap"], r["probs"], pre, np.zeros((w.T, 1), np.uint8), r["cap"], w.E, w.K)
+    o_full = np.zeros((r["cap"], w.H), np.uint16)
+    o_full[sel] = ob
+    yref = oracle.combine(o_full, pre["row_of"][toks], po)
+    o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"][toks], po)
+    assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"][torch.from_numpy(toks).cuda()])),
+                         oracle.bf16_to_f64(yref), o_rows, wts) <= TOL_FP4
