@@ -821,7 +821,7 @@ def main():
     ap.add_argument("--cpu-sample-tokens", type=int, default=16, help="batch-size scale of the CPU oracle sample")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="the CPU oracle baseline samples batches until its MLP + combine part took this long")
-    ap.add_argument("--ref-sample-tokens", type=int, default=1,
+    ap.add_argument("--ref-sample-tokens", type=int, default=16,
                     help="tokens the reference arm (the CPU oracle) runs through the MLP per timed step")
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=INT",
                     help="shrink the workload for profiling captures, e.g. --set E=32 --set T=1024")

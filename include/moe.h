@@ -254,6 +254,51 @@ MOE_API moe_status moe_combine_unpermute(const moe_handle_dev* handle, const moe
                                  const moe_layout* layout, const void* expert_out,
                                  const float* perm_probs, void* y, void* stream);
 
+/* --------------------------------------------------------------- backward */
+
+/* Backward of moe_combine_unpermute ([ALLGATHER], Testing / Output and gradient
+ * regression: hidden-state and probability gradients of the combine;
+ * [SYNC-FREE], What does this PR do?: the combine's backward is a dispatch sized
+ * by the same host capacity).  For the output gradient grad_y and every kept
+ * route (t,k) -> r = row_of[t*K+k] >= 0:
+ *   grad_expert_out[r] = bf16( w(r) * grad_y[t] )   (fp32 product, rounded once)
+ *   grad_perm_probs[r] = sum_h grad_y[t][h] * expert_out[r][h]   (fp32)
+ * with w(r) = perm_probs[r], or 1 when perm_probs is NULL.  Pad rows
+ * [offsets[e]+count[e], offsets[e+1]) below the capacity get zero gradient rows
+ * and zero probability gradients; rows at or beyond min(offsets[E], cap) are
+ * not touched.
+ * grad_y: device bf16 [T][H]; expert_out: device bf16 [cap][H] (the combine's
+ * input; required when grad_perm_probs is non-NULL, else ignored);
+ * perm_probs: device float [cap] or NULL; grad_expert_out: device bf16
+ * [cap][H]; grad_perm_probs: device float [cap] or NULL (not formed).
+ * Errors: MOE_ERR_INVALID_ARG for a NULL or misaligned row buffer, or
+ * grad_perm_probs without expert_out and perm_probs. */
+MOE_API moe_status moe_combine_backward(const moe_handle_dev* handle, const moe_shape* shape,
+                                        const moe_layout* layout, const void* grad_y, const void* expert_out,
+                                        const float* perm_probs, void* grad_expert_out, float* grad_perm_probs,
+                                        void* stream);
+
+/* Backward of moe_dispatch_permute for bf16 rows ([ALLGATHER], Testing / Output
+ * and gradient regression: hidden-state and probability gradients of the
+ * dispatch).  For row gradients grad_perm_tokens and probability gradients
+ * grad_perm_probs of the dispatched rows:
+ *   grad_x[t] = bf16( sum over k ascending with r = row_of[t*K+k] >= 0 of
+ *               grad_perm_tokens[r] )   (fp32 accumulation; a token whose
+ *               routes were all dropped gets zeros)
+ *   grad_probs(t,k) = grad_perm_probs[r] for a kept route, else 0, written in
+ *               the routing layout of routing_format: MOE_ROUTING_DENSE_I16
+ *               float [T][K]; MOE_ROUTING_SPARSE_BOOL float [T][E] with the
+ *               entry of the route's expert set and every other entry 0.
+ * grad_perm_tokens: device bf16 [cap][H]; grad_perm_probs: device float [cap]
+ * or NULL; grad_x: device bf16 [T][H]; grad_probs: device float or NULL (not
+ * formed; required when grad_perm_probs is given).
+ * Errors: MOE_ERR_INVALID_ARG for a NULL or misaligned row buffer, an unknown
+ * routing format, or exactly one of grad_perm_probs / grad_probs NULL. */
+MOE_API moe_status moe_dispatch_backward(const moe_handle_dev* handle, const moe_shape* shape,
+                                         const moe_layout* layout, int32_t routing_format,
+                                         const void* grad_perm_tokens, const float* grad_perm_probs,
+                                         void* grad_x, float* grad_probs, void* stream);
+
 /* ------------------------------------------------------------ grouped MLP */
 
 /* Device workspace bytes of moe_grouped_mlp: the intermediate activation

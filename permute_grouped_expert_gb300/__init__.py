@@ -87,6 +87,10 @@ _SIGNATURES = {
                              ctypes.c_int32, _P, _P, ctypes.POINTER(_Routing), _P, _P, _P, _P],
     "moe_combine_unpermute": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                               _P, _P, _P, _P],
+    "moe_combine_backward": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
+                             _P, _P, _P, _P, _P, _P],
+    "moe_dispatch_backward": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
+                              ctypes.c_int32, _P, _P, _P, _P, _P],
     "moe_grouped_mlp_workspace_size": [ctypes.POINTER(_Shape), ctypes.POINTER(_Layout), ctypes.c_int32,
                                        ctypes.POINTER(ctypes.c_size_t)],
     "moe_grouped_mlp": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
@@ -306,6 +310,23 @@ def moe_combine_unpermute(handle: Handle, shape: Shape, layout: Layout, expert_o
     _check(_lib.moe_combine_unpermute(ctypes.byref(handle.c()), ctypes.byref(shape.c()), ctypes.byref(layout.c()),
                                       _ptr(expert_out), _ptr(perm_probs), _ptr(y), _stream(stream)),
            "moe_combine_unpermute")
+
+
+def moe_combine_backward(handle: Handle, shape: Shape, layout: Layout, grad_y: torch.Tensor,
+                         expert_out: Optional[torch.Tensor], perm_probs: Optional[torch.Tensor],
+                         grad_expert_out: torch.Tensor, grad_perm_probs: Optional[torch.Tensor] = None,
+                         stream=None) -> None:
+    _check(_lib.moe_combine_backward(ctypes.byref(handle.c()), ctypes.byref(shape.c()), ctypes.byref(layout.c()),
+                                     _ptr(grad_y), _ptr(expert_out), _ptr(perm_probs), _ptr(grad_expert_out),
+                                     _ptr(grad_perm_probs), _stream(stream)), "moe_combine_backward")
+
+
+def moe_dispatch_backward(handle: Handle, shape: Shape, layout: Layout, routing_format: int,
+                          grad_perm_tokens: torch.Tensor, grad_perm_probs: Optional[torch.Tensor],
+                          grad_x: torch.Tensor, grad_probs: Optional[torch.Tensor] = None, stream=None) -> None:
+    _check(_lib.moe_dispatch_backward(ctypes.byref(handle.c()), ctypes.byref(shape.c()), ctypes.byref(layout.c()),
+                                      routing_format, _ptr(grad_perm_tokens), _ptr(grad_perm_probs), _ptr(grad_x),
+                                      _ptr(grad_probs), _stream(stream)), "moe_dispatch_backward")
 
 
 def moe_profile_next_grouped_mlp(ev_before_fc1, ev_after_fc1, ev_after_fc2) -> None:

@@ -242,6 +242,39 @@ moe_status moe_combine_unpermute(const moe_handle_dev* handle, const moe_shape* 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+moe_status moe_combine_backward(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
+                                const void* grad_y, const void* expert_out, const float* perm_probs,
+                                void* grad_expert_out, float* grad_perm_probs, void* stream) {
+  MOE_TRY(check_handle(handle));
+  MOE_TRY(check_shape(shape, true));
+  MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
+  if ((shape->T > 0 && !grad_y) || !grad_expert_out || !aligned16(grad_y) || !aligned16(grad_expert_out))
+    return MOE_ERR_INVALID_ARG;
+  if (grad_perm_probs && (!expert_out || !perm_probs || !aligned16(expert_out))) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_combine_backward(*handle, *shape, *layout, grad_y, grad_perm_probs ? expert_out : nullptr,
+                                          perm_probs, grad_expert_out, grad_perm_probs,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status moe_dispatch_backward(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
+                                 int32_t routing_format, const void* grad_perm_tokens, const float* grad_perm_probs,
+                                 void* grad_x, float* grad_probs, void* stream) {
+  MOE_TRY(check_handle(handle));
+  MOE_TRY(check_shape(shape, true));
+  MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
+  if (routing_format != MOE_ROUTING_DENSE_I16 && routing_format != MOE_ROUTING_SPARSE_BOOL)
+    return MOE_ERR_INVALID_ARG;
+  if (!grad_perm_tokens || (shape->T > 0 && !grad_x) || !aligned16(grad_perm_tokens) || !aligned16(grad_x))
+    return MOE_ERR_INVALID_ARG;
+  if ((grad_perm_probs == nullptr) != (grad_probs == nullptr)) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_dispatch_backward(*handle, *shape, *layout, routing_format, grad_perm_tokens,
+                                           grad_perm_probs, grad_x, grad_probs, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
 moe_status moe_grouped_mlp_workspace_size(const moe_shape* shape, const moe_layout* layout,
                                           int32_t w_dtype, size_t* bytes_out) {
   MOE_TRY(check_shape(shape, true));

@@ -55,6 +55,14 @@ cudaError_t launch_combine(const moe_handle_dev& h, const moe_shape& s, const mo
                            const void* expert_out, const float* perm_probs, void* y,
                            cudaStream_t st);
 
+cudaError_t launch_combine_backward(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                                    const void* grad_y, const void* expert_out, const float* perm_probs,
+                                    void* grad_expert_out, float* grad_perm_probs, cudaStream_t st);
+cudaError_t launch_dispatch_backward(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
+                                     int32_t routing_format, const void* grad_perm_tokens,
+                                     const float* grad_perm_probs, void* grad_x, float* grad_probs,
+                                     cudaStream_t st);
+
 cudaError_t launch_quantize_fp8_blocks(const void* w, int64_t G, int64_t N, int64_t Kd, void* codes,
                                        float* scales, cudaStream_t st);
 cudaError_t launch_quantize_nvfp4_rows(const void* x, int64_t R, int64_t Kd, const float* global,

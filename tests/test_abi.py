@@ -162,6 +162,19 @@ def test_validation_rejects_before_any_launch(moe):
     assert lib.moe_grouped_mlp(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16, fake, None,
                                fake, None, fake, None, None, fake, 8, fake,
                                None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    # backward calls: null gradient buffers, probability gradients without their inputs, unknown routing format
+    assert lib.moe_combine_backward(byref(handle), byref(good_shape), byref(good_layout), fake, fake, fake, None,
+                                    None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_backward(byref(handle), byref(good_shape), byref(good_layout), fake, None, fake, fake,
+                                    fake, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_backward(byref(handle), byref(good_shape), byref(good_layout), fake, fake, None, fake,
+                                    fake, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_backward(byref(handle), byref(good_shape), byref(good_layout), 5, fake, None, fake,
+                                     None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_backward(byref(handle), byref(good_shape), byref(good_layout), 0, fake, fake, fake,
+                                     None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_backward(byref(handle), byref(good_shape), byref(good_layout), 0, None, None, fake,
+                                     None, None) == moe.MOE_ERR_INVALID_ARG
     # combine with a null expert buffer
     assert lib.moe_combine_unpermute(byref(handle), byref(good_shape), byref(good_layout), None, None, fake,
                                      None) == moe.MOE_ERR_INVALID_ARG
