@@ -231,6 +231,80 @@ def grouped_mlp_rows(fmt: int, y, y_scales, H: int, I: int, E: int, offsets, w13
     return out, act
 
 
+MX_E4M3, MX_E2M1 = 0, 1
+
+
+def e8m0_decode(codes: np.ndarray) -> np.ndarray:
+    lib = _load()
+    lib.moe_oracle_e8m0_to_f64.restype = ctypes.c_double
+    lib.moe_oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+    table = np.array([lib.moe_oracle_e8m0_to_f64(c) for c in range(256)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def quantize_mx_rows(x_f32: np.ndarray, elem: int):
+    """fp32 [R, H] -> (codes: E4M3 [R, H] or packed E2M1 [R, H/2], E8M0 scale codes [R, H/32])."""
+    x = _c(x_f32, np.float32)
+    R, H = x.shape
+    codes = np.empty((R, H if elem == MX_E4M3 else H // 2), np.uint8)
+    scales = np.empty((R, H // 32), np.uint8)
+    _load().moe_oracle_quantize_mx_rows(_p(x), ctypes.c_int64(R), ctypes.c_int64(H), ctypes.c_int(elem),
+                                        _p(codes), _p(scales))
+    return codes, scales
+
+
+def mx_decode_rows(codes: np.ndarray, scales: np.ndarray, elem: int) -> np.ndarray:
+    """Decoded float64 values [R, H] of MX rows."""
+    codes = np.asarray(codes, np.uint8)
+    if elem == MX_E4M3:
+        v = e4m3_decode(codes)
+    else:
+        v = e2m1_decode(np.stack([codes & 0xF, codes >> 4], -1).reshape(codes.shape[0], -1))
+    return v * np.repeat(e8m0_decode(scales), 32, axis=1)
+
+
+def grouped_mlp_rows_mx(fmt: int, y, y_scales, H: int, I: int, E: int, offsets, w13, w13_scales, w2,
+                        w2_scales, rows, elem: int, w13_global=None, w2_global=None, fc1_in_global: float = 0.0,
+                        fc2_in_global: float = 0.0):
+    """FFN of the listed rows with FC2 written in an MX combine format: (codes, E8M0 scales)."""
+    lib = _load()
+    dt = np.uint16 if fmt == FMT_BF16 else np.uint8
+    sdt = np.float32 if fmt == FMT_FP8 else np.uint8
+    yv, w13v, w2v = _c(y, dt), _c(w13, dt), _c(w2, dt)
+    ys = _c(y_scales, sdt) if y_scales is not None else None
+    w13s = _c(w13_scales, sdt) if w13_scales is not None else None
+    w2s = _c(w2_scales, sdt) if w2_scales is not None else None
+    g13 = _c(w13_global, np.float32) if w13_global is not None else None
+    g2 = _c(w2_global, np.float32) if w2_global is not None else None
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    codes = np.empty((len(rows), H if elem == MX_E4M3 else H // 2), np.uint8)
+    scales = np.empty((len(rows), H // 32), np.uint8)
+    off = _c(offsets, np.int32)
+    fn = lib.moe_oracle_grouped_mlp_rows_mx
+    fn.argtypes = ([ctypes.c_int] + [ctypes.c_void_p] * 2 + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 7
+                   + [ctypes.c_double] * 2 + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p])
+    rc = fn(fmt, _p(yv), _p(ys), H, I, E, _p(off), _p(w13v), _p(w13s), _p(g13), _p(w2v), _p(w2s), _p(g2),
+            fc1_in_global, fc2_in_global, _p(rows), len(rows), elem, _p(codes), _p(scales))
+    if rc != 0:
+        raise ValueError("a listed row lies in no expert segment")
+    return codes, scales
+
+
+def combine_mx(codes: np.ndarray, scales: np.ndarray, elem: int, row_of: np.ndarray, perm_probs=None):
+    """y[t] = bf16(sum_k w * decoded O[row_of[t, k]]) from MX expert rows."""
+    c = _c(codes, np.uint8)
+    sc = _c(scales, np.uint8)
+    ro = _c(row_of, np.int32)
+    T, K = ro.shape
+    H = sc.shape[1] * 32
+    pp = _c(perm_probs, np.float32)
+    y = np.empty((T, H), np.uint16)
+    _load().moe_oracle_combine_mx(_p(c), _p(sc), ctypes.c_int64(H), ctypes.c_int(elem), _p(ro), ctypes.c_int64(T),
+                                  ctypes.c_int64(K), _p(pp), _p(y))
+    return y
+
+
 def combine(o_bf16: np.ndarray, row_of: np.ndarray, perm_probs=None) -> np.ndarray:
     """y[t] = bf16(sum_k w * O[row_of[t, k]]) over kept routes."""
     o = _c(o_bf16, np.uint16)

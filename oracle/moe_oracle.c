@@ -522,7 +522,7 @@ static double weight_value(const operand* w, const float* globals, int64_t N, in
  * in double and rounds to bf16. */
 static void ffn_row(const operand* yin, int64_t r, int64_t e, int64_t H, int64_t I,
                     const operand* w13, const float* w13_global, const operand* w2,
-                    const float* w2_global, double fc2_in_global, uint16_t* out_row,
+                    const float* w2_global, double fc2_in_global, double* out_acc,
                     double* act_dbg) {
   double* act = (double*)malloc(sizeof(double) * (size_t)I);
   float* actf = (float*)malloc(sizeof(float) * (size_t)I);
@@ -561,7 +561,7 @@ static void ffn_row(const operand* yin, int64_t r, int64_t e, int64_t H, int64_t
   for (int64_t n = 0; n < H; n++) {
     double acc = 0.0;
     for (int64_t j = 0; j < I; j++) acc += act[j] * weight_value(w2, w2_global, H, I, e, n, j);
-    out_row[n] = moe_oracle_f64_to_bf16(acc);
+    out_acc[n] = acc;
   }
   free(act);
   free(actf);
@@ -593,10 +593,131 @@ ORACLE_API int moe_oracle_grouped_mlp_rows(int fmt, const void* y, const void* y
       bad = 1;
       continue;
     }
-    ffn_row(&yin, rows[i], e, H, I, &ow13, w13_global, &ow2, w2_global, fc2_in_global,
-            out + i * H, act_out ? act_out + i * I : NULL);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    ffn_row(&yin, rows[i], e, H, I, &ow13, w13_global, &ow2, w2_global, fc2_in_global, acc,
+            act_out ? act_out + i * I : NULL);
+    for (int64_t n = 0; n < H; n++) out[i * H + n] = moe_oracle_f64_to_bf16(acc[n]);
+    free(acc);
   }
   return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* MX combine formats: E4M3 or E2M1 elements with one E8M0 scale per 32        */
+/* ------------------------------------------------------------------------- */
+
+/* [MEGAMOE], commit list: the combine reads bf16, fp8 or fp4 expert outputs
+ * ("fp8 combine may use the bulk fc2 store"); their scale factors are E8M0
+ * bytes and the fp4 vectors E2M1.  Reading (OCP Microscaling Formats (MX)
+ * v1.0, the format family with E8M0 scales): blocks of 32 consecutive elements
+ * of a row share a scale 2^X stored as the E8M0 code X + 127, with
+ * X = floor(log2(amax)) - emax, emax the exponent of the element format's
+ * largest normal (8 for E4M3, 2 for E2M1), X clamped to [-127, 127]; an
+ * all-zero block takes X = 0.  Each element is x / 2^X rounded to the nearest
+ * code, ties to even, saturating at the largest finite magnitude.  The FC2 sums
+ * are rounded to fp32 (the kernel's accumulator precision) before encoding.
+ * elem: 0 = E4M3 (one code byte per element), 1 = E2M1 (two per byte, the even
+ * element in the low nibble). */
+ORACLE_API double moe_oracle_e8m0_to_f64(uint8_t c) { return c == 255 ? NAN : ldexp(1.0, (int)c - 127); }
+
+static void quant_block_mx(const float* v, int elem, uint8_t* codes, uint8_t* scale_code) {
+  float amax = 0.0f;
+  for (int i = 0; i < 32; i++) {
+    float a = fabsf(v[i]);
+    if (a > amax) amax = a;
+  }
+  int X = 0;
+  if (amax > 0.0f) {
+    int e;
+    frexp((double)amax, &e); /* amax = f * 2^e, f in [0.5, 1): floor(log2(amax)) = e - 1 */
+    X = (e - 1) - (elem == 0 ? 8 : 2);
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+  }
+  for (int i = 0; i < 32; i++) {
+    float q = (float)ldexp((double)v[i], -X); /* exact unless it falls below the fp32 range */
+    codes[i] = elem == 0 ? moe_oracle_f32_to_e4m3(q) : moe_oracle_f32_to_e2m1(q);
+  }
+  *scale_code = (uint8_t)(X + 127);
+}
+
+/* fp32 rows [R][H] -> element codes (E4M3 [R][H] or packed E2M1 [R][H/2]) and
+ * E8M0 scale codes [R][H/32]. */
+ORACLE_API void moe_oracle_quantize_mx_rows(const float* x, int64_t R, int64_t H, int elem, uint8_t* codes,
+                                            uint8_t* scales) {
+  uint8_t q[32];
+  for (int64_t r = 0; r < R; r++)
+    for (int64_t b = 0; b < H / 32; b++) {
+      quant_block_mx(x + r * H + b * 32, elem, q, &scales[r * (H / 32) + b]);
+      for (int i = 0; i < 32; i++) {
+        if (elem == 0)
+          codes[r * H + b * 32 + i] = q[i];
+        else if (i % 2 == 0)
+          codes[r * (H / 2) + b * 16 + i / 2] = (uint8_t)(q[i] | (q[i + 1] << 4));
+      }
+    }
+}
+
+static double mx_value(const uint8_t* codes, const uint8_t* scales, int64_t H, int elem, int64_t r, int64_t i) {
+  double v;
+  if (elem == 0) {
+    v = g_e4m3_value[codes[r * H + i]];
+  } else {
+    uint8_t byte = codes[r * (H / 2) + i / 2];
+    v = g_e2m1_value[(i % 2 == 0) ? (byte & 0xF) : (byte >> 4)];
+  }
+  return v * moe_oracle_e8m0_to_f64(scales[r * (H / 32) + i / 32]);
+}
+
+/* The grouped MLP of moe_oracle_grouped_mlp_rows with FC2 rows written in an MX
+ * combine format instead of bf16: out_codes [nrows][H] (E4M3) or [nrows][H/2]
+ * (E2M1), out_scales [nrows][H/32]. */
+ORACLE_API int moe_oracle_grouped_mlp_rows_mx(int fmt, const void* y, const void* y_scales, int64_t H, int64_t I,
+                                              int64_t E, const int32_t* offsets, const void* w13,
+                                              const void* w13_scales, const float* w13_global, const void* w2,
+                                              const void* w2_scales, const float* w2_global, double fc1_in_global,
+                                              double fc2_in_global, const int64_t* rows, int64_t nrows, int elem,
+                                              uint8_t* out_codes, uint8_t* out_scales) {
+  operand yin = {fmt, y, y_scales, fc1_in_global};
+  operand ow13 = {fmt, w13, w13_scales, 0.0};
+  operand ow2 = {fmt, w2, w2_scales, 0.0};
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int64_t i = 0; i < nrows; i++) {
+    int64_t e = expert_of_row(offsets, E, rows[i]);
+    if (e < 0) {
+      bad = 1;
+      continue;
+    }
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    float* accf = (float*)malloc(sizeof(float) * (size_t)H);
+    ffn_row(&yin, rows[i], e, H, I, &ow13, w13_global, &ow2, w2_global, fc2_in_global, acc, NULL);
+    for (int64_t n = 0; n < H; n++) accf[n] = f64_to_f32(acc[n]);
+    moe_oracle_quantize_mx_rows(accf, 1, H, elem, out_codes + i * (elem == 0 ? H : H / 2), out_scales + i * (H / 32));
+    free(acc);
+    free(accf);
+  }
+  return bad ? -1 : 0;
+}
+
+/* Combine from an MX expert-output buffer: y[t] = bf16( sum over k ascending of
+ * w(r) * decoded O[r] ) over the kept routes, as moe_oracle_combine does for
+ * bf16 rows. */
+ORACLE_API void moe_oracle_combine_mx(const uint8_t* codes, const uint8_t* scales, int64_t H, int elem,
+                                      const int32_t* row_of, int64_t T, int64_t K, const float* perm_probs,
+                                      uint16_t* y) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; t++)
+    for (int64_t h = 0; h < H; h++) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; k++) {
+        int32_t r = row_of[t * K + k];
+        if (r < 0) continue;
+        double w = perm_probs ? (double)perm_probs[r] : 1.0;
+        acc += w * mx_value(codes, scales, H, elem, r, h);
+      }
+      y[t * H + h] = moe_oracle_f64_to_bf16(acc);
+    }
 }
 
 /* ------------------------------------------------------------------------- */
@@ -730,17 +851,17 @@ ORACLE_API int moe_oracle_layer_per_token(int fmt, int format, const void* map, 
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < ntok; i++) {
     int64_t t = tokens[i];
-    uint16_t* tmp = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+    double* row_acc = (double*)malloc(sizeof(double) * (size_t)H);
     double* acc = (double*)calloc((size_t)H, sizeof(double));
     for (int64_t k = 0; k < K; k++) {
       int e = route[t * K + k];
       if (e < 0) continue;
       double p = probs ? prob_of_route(format, probs, t, k, e, E, K) : 1.0;
-      ffn_row(&xin, t, e, H, I, &ow13, w13_global, &ow2, w2_global, fc2_in_global, tmp, NULL);
-      for (int64_t h = 0; h < H; h++) acc[h] += p * moe_oracle_bf16_to_f64(tmp[h]);
+      ffn_row(&xin, t, e, H, I, &ow13, w13_global, &ow2, w2_global, fc2_in_global, row_acc, NULL);
+      for (int64_t h = 0; h < H; h++) acc[h] += p * moe_oracle_bf16_to_f64(moe_oracle_f64_to_bf16(row_acc[h]));
     }
     for (int64_t h = 0; h < H; h++) y[i * H + h] = moe_oracle_f64_to_bf16(acc[h]);
-    free(tmp);
+    free(row_acc);
     free(acc);
   }
   free(route);
