@@ -147,10 +147,14 @@ def job_throughput(tokens_per_rank: int, world: int, steps: int, ms_slowest: flo
 class Problem:
     """Device-resident inputs, outputs and workspaces of one MoE layer."""
 
-    def __init__(self, moe, w: workloads.Workload, seed: int, dev):
+    def __init__(self, moe, w: workloads.Workload, seed: int, dev, combine_format: str = "bf16"):
         import torch
 
         self.moe, self.w, self.dev = moe, w, dev
+        self.cfmt = {"bf16": moe.COMBINE_BF16, "mxfp8": moe.COMBINE_MXFP8, "mxfp4": moe.COMBINE_MXFP4}[combine_format]
+        if self.cfmt != moe.COMBINE_BF16 and w.dtype != "fp8":
+            raise SystemExit("--combine-format mxfp8/mxfp4 is written by the FP8 path's FC2 epilogue only")
+        self.combine_format = combine_format
         fmt, rmap, probs = workloads.routing_inputs(w, seed)
         self.fmt = fmt
         self.map_host = torch.from_numpy(np.ascontiguousarray(rmap)).pin_memory()
@@ -227,7 +231,13 @@ class Problem:
             torch.cuda.empty_cache()  # release the bf16 weight temporaries
             self.act_ws = torch.empty(moe.moe_grouped_mlp_workspace_size(self.shape, self.layout, self.w_dtype),
                                       dtype=torch.uint8, device=dev)
-            self.o = torch.empty(cap, w.H, dtype=torch.bfloat16, device=dev)
+            if self.cfmt == moe.COMBINE_BF16:
+                self.o = torch.empty(cap, w.H, dtype=torch.bfloat16, device=dev)
+                self.o_scales = None
+            else:
+                self.o = torch.empty(cap, w.H if self.cfmt == moe.COMBINE_MXFP8 else w.H // 2, dtype=torch.uint8,
+                                     device=dev)
+                self.o_scales = torch.empty(cap, w.H // 32, dtype=torch.uint8, device=dev)
             self.mlp_kernels = moe.moe_grouped_mlp_kernel_count(self.shape, self.layout, self.w_dtype)
         torch.cuda.synchronize()
 
@@ -250,8 +260,9 @@ class Problem:
         if not self.identity:
             if prof:
                 moe.moe_profile_next_grouped_mlp(*prof)
-            moe.moe_grouped_mlp(self.handle, self.shape, self.layout, self.w_dtype, self.y, self.y_scales, self.w13,
-                                self.w13_s, self.w2, self.w2_s, self.globals, self.act_ws, self.o, stream=stream)
+            moe.moe_grouped_mlp_fmt(self.handle, self.shape, self.layout, self.w_dtype, self.y, self.y_scales,
+                                    self.w13, self.w13_s, self.w2, self.w2_s, self.globals, self.act_ws, self.cfmt,
+                                    self.o, self.o_scales, stream=stream)
         rec(3)
         self.call_combine(stream, slot)
         rec(4)
@@ -267,9 +278,12 @@ class Problem:
 
     def call_combine(self, stream, slot=0):
         io = self.slots[slot]
-        expert_out = self.y if self.identity else self.o
-        self.moe.moe_combine_unpermute(self.handle, self.shape, self.layout, expert_out, self.yp, io["out"],
-                                       stream=stream)
+        if self.identity:
+            self.moe.moe_combine_unpermute(self.handle, self.shape, self.layout, self.y, self.yp, io["out"],
+                                           stream=stream)
+        else:
+            self.moe.moe_combine_unpermute_fmt(self.handle, self.shape, self.layout, self.cfmt, self.o,
+                                               self.o_scales, self.yp, io["out"], stream=stream)
 
     def kernels_per_step(self) -> int:
         return 2 + 1 + (0 if self.identity else self.mlp_kernels) + 1
@@ -304,12 +318,21 @@ class Problem:
         wb = self._elem_bytes(2 * w.I * w.H)
         return active * wb + R * self._elem_bytes(w.H) + R * self._elem_bytes(w.I)
 
+    def out_row_bytes(self):
+        """Bytes of one expert-output row in the combine format."""
+        w = self.w
+        if getattr(self, "combine_format", "bf16") == "mxfp8":
+            return w.H + w.H // 32
+        if getattr(self, "combine_format", "bf16") == "mxfp4":
+            return w.H // 2 + w.H // 32
+        return 2 * w.H
+
     def fc2_bytes(self, R, active):
-        """FC2 algorithmic bytes: the active experts' w2, the intermediate read, the bf16 output written."""
+        """FC2 algorithmic bytes: the active experts' w2, the intermediate read, the output rows written."""
         w = self.w
         if w.dtype == "fp8":
             wb = w.H * w.I + 4 * (w.H // 128) * (w.I // 128)
-            return active * wb + R * (w.I + 4 * w.I // 128) + R * 2 * w.H
+            return active * wb + R * (w.I + 4 * w.I // 128) + R * self.out_row_bytes()
         return active * self._elem_bytes(w.H * w.I) + R * self._elem_bytes(w.I) + R * 2 * w.H
 
     def dispatch_bytes(self, R):
@@ -320,7 +343,7 @@ class Problem:
 
     def combine_bytes(self, R):
         w = self.w
-        return R * 2 * w.H + R * 4 + w.T * w.K * 4 + w.T * 2 * w.H
+        return R * self.out_row_bytes() + R * 4 + w.T * w.K * 4 + w.T * 2 * w.H
 
 
 def make_prof_events(n, stream):
@@ -400,7 +423,7 @@ def run_ours(args, w):
         dist.barrier()
     import permute_grouped_expert_gb300 as moe
 
-    prob = Problem(moe, w, args.seed + rank, dev)
+    prob = Problem(moe, w, args.seed + rank, dev, args.combine_format)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
 
@@ -619,6 +642,7 @@ def run_ours(args, w):
         "dtype": w.dtype, "data": "synthetic (seeded; shapes of the pages' workloads)",
         "config": {"workload": w.name, "tokens": w.T, "hidden": w.H, "experts": w.E, "topk": w.K,
                    "intermediate": w.I, "pad_multiple": w.m, "routing": w.routing,
+                   "combine_format": args.combine_format,
                    "capacity_factor": w.cap_factor or None, "capacity": prob.cap,
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2)"
                    if in_bytes > L2_BYTES else "inputs smaller than L2 (no flush)",
@@ -816,6 +840,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="dsv3", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--combine-format", default="bf16", choices=["bf16", "mxfp8", "mxfp4"],
+                    help="format of the expert-output rows the combine reads (MX formats: FP8 path only)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16, help="batch-size scale of the CPU oracle sample")

@@ -106,6 +106,21 @@ enum {
   MOE_DTYPE_BF16_TO_NVFP4 = 4    /* dispatch only: bf16 input quantized to NVFP4 */
 };
 
+/* Formats of expert-output rows read by the combine ([MEGAMOE], commit list:
+ * bf16 / fp8 / fp4 combine formats with E8M0 scale factors and E2M1 fp4
+ * vectors).  MX formats (the OCP Microscaling family, whose scales are E8M0):
+ * blocks of 32 consecutive elements of a row share a scale 2^X stored as the
+ * byte X + 127, X = floor(log2(amax)) - emax (emax 8 for E4M3, 2 for E2M1)
+ * clamped to [-127, 127], 0 for an all-zero block; each element is x / 2^X
+ * rounded to nearest even and saturated.  Row layouts: MXFP8 codes [cap][H]
+ * bytes, MXFP4 packed [cap][H/2] (even element in the low nibble); scales
+ * [cap][H/32] bytes. */
+enum {
+  MOE_COMBINE_BF16 = 0,   /* bf16 [cap][H] */
+  MOE_COMBINE_MXFP8 = 1,  /* E4M3 + E8M0 per 32 */
+  MOE_COMBINE_MXFP4 = 2   /* E2M1 + E8M0 per 32 */
+};
+
 /* Bits of the device status word handle->status. */
 #define MOE_DEV_ERR_BAD_EXPERT 1      /* a dense id outside [-1, E): treated as no route */
 #define MOE_DEV_ERR_TOO_MANY_ROUTES 2 /* a sparse row with more than K routed experts:
@@ -158,6 +173,20 @@ MOE_API moe_status moe_capacity(int64_t rows, double factor, int64_t align, int6
 /* Bytes of a routing map ([ALLGATHER], Memory impact): T*E for the sparse
  * Boolean layout, T*K*2 for dense int16 ids.  Host only. */
 MOE_API moe_status moe_routing_map_bytes(int32_t format, int64_t T, int64_t E, int64_t K, size_t* bytes_out);
+
+/* Decode-bucket selection ([MEGAMOE], commit list: adaptive max-tokens
+ * bucketing, so that a decode batch launches kernels sized for a small bucket
+ * instead of the prefill maximum; the full bucket is kept for zero tokens so
+ * no launch has an empty grid; a batch above the largest bucket is an error).
+ * ladder: n >= 1 strictly increasing positive token counts (host array), the
+ * shapes a caller has sized buffers for and captured graphs at.  Returns in
+ * *bucket_out the smallest ladder entry >= max(tokens, 1).  The caller runs
+ * the layer at T = bucket with the extra tokens' routing set to "no route"
+ * (dense id -1, or an all-zero sparse row): they get no rows, and every real
+ * token's results are those of the unpadded batch.  Host only.  Errors:
+ * MOE_ERR_INVALID_ARG for tokens < 0, tokens above ladder[n-1], or a ladder
+ * that is empty, unsorted or not positive. */
+MOE_API moe_status moe_decode_bucket(int64_t tokens, const int64_t* ladder, int32_t n, int64_t* bucket_out);
 
 /* Message of the last CUDA error seen by this thread's library calls. */
 MOE_API const char* moe_last_cuda_error(void);
@@ -254,6 +283,25 @@ MOE_API moe_status moe_combine_unpermute(const moe_handle_dev* handle, const moe
                                  const moe_layout* layout, const void* expert_out,
                                  const float* perm_probs, void* y, void* stream);
 
+/* combine with unpermutation from expert rows in a combine format: as
+ * moe_combine_unpermute, with the expert rows decoded from in_format
+ * (MOE_COMBINE_BF16 reads expert_out as bf16 and ignores expert_out_scales;
+ * the MX formats read codes from expert_out and E8M0 scales from
+ * expert_out_scales, layouts as documented with MOE_COMBINE_*):
+ *   y[t] = bf16( sum over k ascending of w(r) * decoded O[r] ), fp32 accumulation.
+ * Errors: MOE_ERR_INVALID_ARG for an unknown format or a NULL / misaligned
+ * buffer (expert_out and y 16-byte aligned). */
+MOE_API moe_status moe_combine_unpermute_fmt(const moe_handle_dev* handle, const moe_shape* shape,
+                                             const moe_layout* layout, int32_t in_format, const void* expert_out,
+                                             const void* expert_out_scales, const float* perm_probs, void* y,
+                                             void* stream);
+
+/* bf16 rows [R][H] (H a multiple of 32) -> a combine format's codes and E8M0
+ * scales (format MOE_COMBINE_MXFP8 or MOE_COMBINE_MXFP4; layouts as documented
+ * with MOE_COMBINE_*).  For expert outputs that were written in bf16. */
+MOE_API moe_status moe_quantize_mx_rows(const void* x, int64_t R, int64_t H, int32_t format, void* codes,
+                                        void* scales, void* stream);
+
 /* --------------------------------------------------------------- backward */
 
 /* Backward of moe_combine_unpermute ([ALLGATHER], Testing / Output and gradient
@@ -342,6 +390,23 @@ MOE_API moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape
                            const void* w13, const void* w13_scales, const void* w2,
                            const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
                            size_t workspace_bytes, void* out_fc2, void* stream);
+
+/* moe_grouped_mlp with FC2 rows written in a combine format ([MEGAMOE], commit
+ * list: "fp8 combine may use the bulk fc2 store"): out_format
+ * MOE_COMBINE_BF16 behaves exactly as moe_grouped_mlp (out_fc2_scales
+ * ignored); MOE_COMBINE_MXFP8 / MOE_COMBINE_MXFP4 make FC2's epilogue encode
+ * each row's fp32 sums into codes at out_fc2 and E8M0 scales at out_fc2_scales
+ * (device [cap][H/32] bytes, 4-byte aligned), layouts as documented with
+ * MOE_COMBINE_*.  The MX formats are written by the FP8 path
+ * (w_dtype MOE_DTYPE_FP8_E4M3_B128); other w_dtype values return
+ * MOE_ERR_UNSUPPORTED with them (write bf16 and convert with
+ * moe_quantize_mx_rows). */
+MOE_API moe_status moe_grouped_mlp_fmt(const moe_handle_dev* handle, const moe_shape* shape,
+                                       const moe_layout* layout, int32_t w_dtype, const void* perm_tokens,
+                                       const void* perm_scales, const void* w13, const void* w13_scales,
+                                       const void* w2, const void* w2_scales, const moe_nvfp4_globals* globals,
+                                       void* workspace, size_t workspace_bytes, int32_t out_format, void* out_fc2,
+                                       void* out_fc2_scales, void* stream);
 
 /* Number of kernels one moe_grouped_mlp call with these arguments launches
  * (host only, no device access): 1 where FC1 and FC2 run in one persistent

@@ -42,6 +42,10 @@ DTYPE_BF16_TO_FP8 = 2
 DTYPE_NVFP4 = 3
 DTYPE_BF16_TO_NVFP4 = 4
 
+COMBINE_BF16 = 0
+COMBINE_MXFP8 = 1
+COMBINE_MXFP4 = 2
+
 DEV_ERR_BAD_EXPERT = 1
 DEV_ERR_TOO_MANY_ROUTES = 2
 DEV_ERR_TIMEOUT = 4
@@ -76,6 +80,7 @@ _I64 = ctypes.c_int64
 _SIGNATURES = {
     "moe_capacity": [_I64, ctypes.c_double, _I64, ctypes.POINTER(_I64)],
     "moe_routing_map_bytes": [ctypes.c_int32, _I64, _I64, _I64, ctypes.POINTER(ctypes.c_size_t)],
+    "moe_decode_bucket": [_I64, ctypes.POINTER(_I64), ctypes.c_int32, ctypes.POINTER(_I64)],
     "moe_last_cuda_error": [],
     "moe_status_string": [ctypes.c_int],
     "moe_preprocess_workspace_size": [ctypes.POINTER(_Shape), ctypes.POINTER(ctypes.c_size_t)],
@@ -96,6 +101,12 @@ _SIGNATURES = {
     "moe_grouped_mlp": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                         ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Nvfp4Globals), _P,
                         ctypes.c_size_t, _P, _P],
+    "moe_grouped_mlp_fmt": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
+                            ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Nvfp4Globals), _P,
+                            ctypes.c_size_t, ctypes.c_int32, _P, _P, _P],
+    "moe_combine_unpermute_fmt": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
+                                  ctypes.c_int32, _P, _P, _P, _P, _P],
+    "moe_quantize_mx_rows": [_P, _I64, _I64, ctypes.c_int32, _P, _P, _P],
     "moe_grouped_mlp_kernel_count": [ctypes.POINTER(_Shape), ctypes.POINTER(_Layout), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_int32)],
     "moe_profile_next_grouped_mlp": [_P, _P, _P],
@@ -237,6 +248,14 @@ def moe_capacity(rows: int, factor: float, align: int = 4) -> int:
     return out.value
 
 
+def moe_decode_bucket(tokens: int, ladder) -> int:
+    """Smallest bucket of ``ladder`` (ascending token counts) that holds ``tokens``."""
+    arr = (_I64 * len(ladder))(*ladder)
+    out = _I64()
+    _check(_lib.moe_decode_bucket(tokens, arr, len(ladder), ctypes.byref(out)), "moe_decode_bucket")
+    return out.value
+
+
 def moe_routing_map_bytes(fmt: int, T: int, E: int, K: int) -> int:
     out = ctypes.c_size_t()
     _check(_lib.moe_routing_map_bytes(fmt, T, E, K, ctypes.byref(out)), "moe_routing_map_bytes")
@@ -303,6 +322,35 @@ def moe_grouped_mlp(handle: Handle, shape: Shape, layout: Layout, w_dtype: int, 
                                 _ptr(w2), _ptr(w2_scales), g, _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _ptr(out_fc2), _stream(stream)),
            "moe_grouped_mlp")
+
+
+def moe_grouped_mlp_fmt(handle: Handle, shape: Shape, layout: Layout, w_dtype: int, perm_tokens: torch.Tensor,
+                        perm_scales: Optional[torch.Tensor], w13: torch.Tensor, w13_scales: Optional[torch.Tensor],
+                        w2: torch.Tensor, w2_scales: Optional[torch.Tensor], globals_: Optional[Nvfp4Globals],
+                        workspace: torch.Tensor, out_format: int, out_fc2: torch.Tensor,
+                        out_fc2_scales: Optional[torch.Tensor], stream=None) -> None:
+    g = ctypes.byref(globals_.c()) if globals_ is not None else None
+    _check(_lib.moe_grouped_mlp_fmt(ctypes.byref(handle.c()), ctypes.byref(shape.c()), ctypes.byref(layout.c()),
+                                    w_dtype, _ptr(perm_tokens), _ptr(perm_scales), _ptr(w13), _ptr(w13_scales),
+                                    _ptr(w2), _ptr(w2_scales), g, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), out_format, _ptr(out_fc2),
+                                    _ptr(out_fc2_scales), _stream(stream)), "moe_grouped_mlp_fmt")
+
+
+def moe_combine_unpermute_fmt(handle: Handle, shape: Shape, layout: Layout, in_format: int,
+                              expert_out: torch.Tensor, expert_out_scales: Optional[torch.Tensor],
+                              perm_probs: Optional[torch.Tensor], y: torch.Tensor, stream=None) -> None:
+    _check(_lib.moe_combine_unpermute_fmt(ctypes.byref(handle.c()), ctypes.byref(shape.c()),
+                                          ctypes.byref(layout.c()), in_format, _ptr(expert_out),
+                                          _ptr(expert_out_scales), _ptr(perm_probs), _ptr(y), _stream(stream)),
+           "moe_combine_unpermute_fmt")
+
+
+def moe_quantize_mx_rows(x: torch.Tensor, fmt: int, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    H = x.shape[-1]
+    R = x.numel() // H
+    _check(_lib.moe_quantize_mx_rows(_ptr(x), R, H, fmt, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_quantize_mx_rows")
 
 
 def moe_combine_unpermute(handle: Handle, shape: Shape, layout: Layout, expert_out: torch.Tensor,

@@ -106,37 +106,82 @@ struct Fp8Params {
   int64_t b_rows_per_expert; // 2I (FC1) or H (FC2)
   int64_t gate_offset;       // FC1: I (rows of w1 after w3)
   int E, cap, nt, nkb, n_blocks_b;  // n_blocks_b = weight rows / 128 per expert
+  int out_format;            // FC2: MOE_COMBINE_BF16 / _MXFP8 / _MXFP4
+  uint8_t* out_mx_scales;    // FC2 in an MX format: E8M0 [cap][H/32]
 };
+
+// Shared exponent X of an MX block with magnitude maximum amax: floor(log2(amax))
+// - emax (8 for E4M3, 2 for E2M1) from the fp32 bits, clamped to [-127, 127];
+// 0 for an all-zero block.
+MOE_DEVICE int mx_exponent(float amax, int emax) {
+  if (amax == 0.0f) return 0;
+  const int field = (int)((__float_as_uint(amax) >> 23) & 0xff);  // 0 for a subnormal: floor(log2) <= -127
+  const int X = (field == 0 ? -127 : field - 127) - emax;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
 
 struct TileInfo {
   int e, m, n;
   int64_t row0, row_end;
+  bool shares_b;  // the pair shares the weight tile (two M tiles), else the token tile (two N tiles)
+  bool masked;    // the second tile of a pair past the last N tile: computed, never stored
 };
 
-__device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const int* mt, const Fp8Params& p) {
+// Work units of a CTA pair.  Expert e with mt token tiles and nt output tiles
+// has (mt / 2) * nt units of two token tiles (m, m+1) that share one weight
+// tile, and, for an odd mt, ceil(nt / 2) units of two output tiles (n, n+1)
+// of its last token tile that share the token tile.  CTA `rank` of the pair
+// takes the unit's tile number `rank`.  Within an expert the units sharing a
+// weight tile come first, token-tile pairs innermost, so neighbouring CTA
+// pairs read the same weight tile while it is in L2.
+__device__ __forceinline__ int units_of(int mt, int nt) { return (mt / 2) * nt + (mt & 1) * ((nt + 1) / 2); }
+
+__device__ __forceinline__ TileInfo decode_unit(int u, uint32_t rank, const int* prefix, const int* mt,
+                                                const Fp8Params& p) {
   int lo = 0, hi = p.E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= t)
+    if (prefix[mid] <= u)
       lo = mid;
     else
       hi = mid - 1;
   }
   TileInfo ti;
   ti.e = lo;
-  const int local = t - prefix[lo];
-  ti.n = local / mt[lo];
-  ti.m = local % mt[lo];
+  const int local = u - prefix[lo];
+  const int mpairs = mt[lo] / 2;
+  ti.masked = false;
+  if (local < mpairs * p.nt) {
+    ti.shares_b = true;
+    ti.n = local / mpairs;
+    ti.m = 2 * (local % mpairs) + (int)rank;
+  } else {
+    ti.shares_b = false;
+    ti.m = mt[lo] - 1;
+    ti.n = 2 * (local - mpairs * p.nt) + (int)rank;
+    if (ti.n >= p.nt) {
+      ti.n = p.nt - 1;
+      ti.masked = true;
+    }
+  }
   const int64_t seg_b = min64(p.offsets[lo], p.cap);
   ti.row_end = min64(p.offsets[lo + 1], p.cap);
   ti.row0 = seg_b + (int64_t)ti.m * BM;
   return ti;
 }
 
+// Spin (bounded) until `ns` nanoseconds have passed: lets this CTA's own
+// multicast copies land after an abort, when part of their completion is
+// counted on the peer's barriers and cannot be observed here.
+__device__ __forceinline__ void settle(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
+}
+
 template <int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                            Fp8Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a64,
+                            const __grid_constant__ CUtensorMap tm_b, Fp8Params p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_pfull[2], s_pempty[2], s_drain;
   __shared__ uint32_t s_tmem;
@@ -148,13 +193,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   volatile int* abort_flag = &s_abort;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int s = 0; s < kStages; s++) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 1);
+      mbar_init(&s_full[s], 1);   // own producer's arrive; bytes from both CTAs' copies
+      mbar_init(&s_empty[s], 2);  // both CTAs' MMA commits: the peer's copies also write this stage
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(&s_pfull[b], 1);
@@ -165,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s_xbar[1], kEpiWarps);
     fence_barrier_init();
     tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_a64);
     tma_prefetch_desc(&tm_b);
   }
   if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
@@ -177,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t b = min64(p.offsets[e], p.cap), en = min64(p.offsets[e + 1], p.cap);
         const int m = en > b ? (int)((en - b + BM - 1) / BM) : 0;
         s_mt[e] = m;
-        local += m;
+        local += units_of(m, p.nt);
       }
     }
     int incl = local;
@@ -190,14 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < per; j++) {
       const int e = lane * per + j;
       if (e < p.E) {
-        s_prefix[e] = run * p.nt;
-        run += s_mt[e];
+        s_prefix[e] = run;
+        run += units_of(s_mt[e], p.nt);
       }
     }
-    if (lane == 31) s_prefix[p.E] = incl * p.nt;
+    if (lane == 31) s_prefix[p.E] = incl;
   }
+  // both CTAs' barriers exist before either CTA's copies or commits reach the peer
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
   const int total = s_prefix[p.E];
@@ -211,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued[kStages];
       for (int s = 0; s < kStages; s++) issued[s] = false;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(t, s_prefix, s_mt, p);
+      for (int u = cluster; u < total && ok; u += nclusters) {
+        const TileInfo ti = decode_unit(u, rank, s_prefix, s_mt, p);
         const int64_t ebase = (int64_t)ti.e * p.b_rows_per_expert;
         for (int kb = 0; kb < p.nkb; kb++) {
           if (!mbar_wait(&s_empty[stage], phase ^ 1, abort_flag, p.status)) {
@@ -221,22 +271,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + (size_t)stage * kStageBytes;
           uint8_t* sb = sa + kTileABytes;
+          // every stage receives a whole A and B tile in each CTA: this CTA's own
+          // operand, half of the shared one from each CTA of the pair
           mbar_arrive_expect_tx(&s_full[stage], kStageBytes);
-          tma_load_2d(sa, &tm_a, kb * BK, (int32_t)ti.row0, &s_full[stage]);
-          if (kMode == kFc1SwiGLU) {
-            // 64-row boxes: up[0:64), gate[0:64), up[64:128), gate[64:128) of this 128-column tile
-            const int64_t up = ebase + (int64_t)ti.n * 128, gate = up + p.gate_offset;
-            tma_load_2d(sb + 0 * 8192, &tm_b, kb * BK, (int32_t)up, &s_full[stage]);
-            tma_load_2d(sb + 1 * 8192, &tm_b, kb * BK, (int32_t)gate, &s_full[stage]);
-            tma_load_2d(sb + 2 * 8192, &tm_b, kb * BK, (int32_t)(up + 64), &s_full[stage]);
-            tma_load_2d(sb + 3 * 8192, &tm_b, kb * BK, (int32_t)(gate + 64), &s_full[stage]);
+          if (ti.shares_b) {
+            tma_load_2d(sa, &tm_a, kb * BK, (int32_t)ti.row0, &s_full[stage]);
+            if (kMode == kFc1SwiGLU) {
+              // 64-row boxes up[0:64), gate[0:64), up[64:128), gate[64:128): this CTA loads pair `rank`
+              const int64_t up = ebase + (int64_t)ti.n * 128 + 64 * rank, gate = up + p.gate_offset;
+              tma_load_2d_mc(sb + (2 * rank) * 8192, &tm_b, kb * BK, (int32_t)up, &s_full[stage], 0x3);
+              tma_load_2d_mc(sb + (2 * rank + 1) * 8192, &tm_b, kb * BK, (int32_t)gate, &s_full[stage], 0x3);
+            } else {
+              const int64_t r0 = ebase + (int64_t)ti.n * BN + 128 * rank;
+              tma_load_2d_mc(sb + rank * (kTileBBytes / 2), &tm_b, kb * BK, (int32_t)r0, &s_full[stage], 0x3);
+            }
           } else {
-            const int64_t r0 = ebase + (int64_t)ti.n * BN;
-            tma_load_2d(sb, &tm_b, kb * BK, (int32_t)r0, &s_full[stage]);
-            tma_load_2d(sb + kTileBBytes / 2, &tm_b, kb * BK, (int32_t)(r0 + 128), &s_full[stage]);
+            // rows [64 rank, 64 rank + 64) of the shared token tile
+            tma_load_2d_mc(sa + rank * (kTileABytes / 2), &tm_a64, kb * BK, (int32_t)(ti.row0 + 64 * rank),
+                           &s_full[stage], 0x3);
+            if (kMode == kFc1SwiGLU) {
+              const int64_t up = ebase + (int64_t)ti.n * 128, gate = up + p.gate_offset;
+              tma_load_2d(sb + 0 * 8192, &tm_b, kb * BK, (int32_t)up, &s_full[stage]);
+              tma_load_2d(sb + 1 * 8192, &tm_b, kb * BK, (int32_t)gate, &s_full[stage]);
+              tma_load_2d(sb + 2 * 8192, &tm_b, kb * BK, (int32_t)(up + 64), &s_full[stage]);
+              tma_load_2d(sb + 3 * 8192, &tm_b, kb * BK, (int32_t)(gate + 64), &s_full[stage]);
+            } else {
+              const int64_t r0 = ebase + (int64_t)ti.n * BN;
+              tma_load_2d(sb, &tm_b, kb * BK, (int32_t)r0, &s_full[stage]);
+              tma_load_2d(sb + kTileBBytes / 2, &tm_b, kb * BK, (int32_t)(r0 + 128), &s_full[stage]);
+            }
           }
           issued[stage] = true;
           issued_parity[stage] = phase;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (ok) {
+        // every stage this CTA filled (here and, by multicast, in the peer) has
+        // been released by both CTAs' MMAs: no copy or commit of this pair is
+        // still on its way to either CTA when they leave
+        for (int s = 0; s < kStages && ok; s++) {
+          if (!mbar_wait(&s_empty[stage], phase ^ 1, abort_flag, p.status)) ok = false;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -250,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (!mbar_try_wait(&s_full[s], issued_parity[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
         }
+        settle(2000000);  // 2 ms: far longer than any single copy takes
       }
     }
   } else if (warp == 1) {
@@ -259,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, buf = 0;
       uint32_t phase = 0, buf_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int u = cluster; u < total && ok; u += nclusters) {
         for (int kb = 0; kb < p.nkb; kb++) {
           if (!mbar_wait(&s_pempty[buf], buf_phase ^ 1, abort_flag, p.status) ||
               !mbar_wait(&s_full[stage], phase, abort_flag, p.status)) {
@@ -273,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
 #pragma unroll
           for (int k = 0; k < BK / 32; k++) mma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0 ? 1u : 0u);
-          mma_commit(&s_empty[stage]);
+          mma_commit_mc(&s_empty[stage], 0x3);  // releases the stage in both CTAs
           mma_commit(&s_pfull[buf]);
           if (++stage == kStages) {
             stage = 0;
@@ -304,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t buf_phase = 0;
     int tile_iter = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, tile_iter++) {
-      const TileInfo ti = decode_tile(t, s_prefix, s_mt, p);
+    for (int u = cluster; u < total && ok; u += nclusters, tile_iter++) {
+      const TileInfo ti = decode_unit(u, rank, s_prefix, s_mt, p);
       const int64_t row = ti.row0 + r_local;
       const bool row_in = row < p.cap;
       const float* arow = p.a_scales + (row_in ? row : 0) * (int64_t)nsb;
@@ -363,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      const bool valid = row < ti.row_end;
+      const bool valid = row < ti.row_end && !ti.masked;
       float* acc = reinterpret_cast<float*>(acc2);
       if (kMode == kFc1SwiGLU) {
         // acc[0..63] = up, acc[64..127] = gate of output columns n*128 + 64*grp + j
@@ -401,6 +480,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (grp == 0) p.out_scales[row * (p.ld_out / 128) + ti.n] = s;
         }
+      } else if (p.out_format != MOE_COMBINE_BF16) {
+        // MX combine format: the thread's 128 columns are four blocks of 32,
+        // each with its E8M0 scale; x / 2^X is exact in fp32, then rounded
+        // to the element format (nearest even, saturating)
+        const int64_t col0 = (int64_t)ti.n * BN + grp * 128;
+        if (valid && col0 < p.out_cols) {
+          const bool fp8 = p.out_format == MOE_COMBINE_MXFP8;
+          uint32_t sc4 = 0;
+#pragma unroll
+          for (int b = 0; b < 4; b++) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; j++) amax = fmaxf(amax, fabsf(acc[32 * b + j]));
+            const int X = mx_exponent(amax, fp8 ? 8 : 2);
+            sc4 |= (uint32_t)(X + 127) << (8 * b);
+            const float inv = X < 127 ? __uint_as_float((uint32_t)(127 - X) << 23) : __uint_as_float(0x00400000u);
+            if (fp8) {
+              uint8_t* dst = p.out + row * p.ld_out + col0 + 32 * b;
+#pragma unroll
+              for (int q = 0; q < 2; q++) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                  const int j = 32 * b + 16 * q + 4 * i;
+                  w4[i] = (uint32_t)e4m3x2(acc[j] * inv, acc[j + 1] * inv) |
+                          ((uint32_t)e4m3x2(acc[j + 2] * inv, acc[j + 3] * inv) << 16);
+                }
+                *reinterpret_cast<uint4*>(dst + 16 * q) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            } else {
+              uint32_t w4[4] = {0, 0, 0, 0};
+#pragma unroll
+              for (int j = 0; j < 16; j++)
+                w4[j >> 2] |= e2m1x2(acc[32 * b + 2 * j] * inv, acc[32 * b + 2 * j + 1] * inv) << (8 * (j & 3));
+              *reinterpret_cast<uint4*>(p.out + row * (p.ld_out / 2) + (col0 + 32 * b) / 2) =
+                  make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+          *reinterpret_cast<uint32_t*>(p.out_mx_scales + row * (p.ld_out / 32) + col0 / 32) = sc4;
+        }
       } else {
         const int64_t col0 = (int64_t)ti.n * BN + grp * 128;
         if (valid && col0 < p.out_cols) {
@@ -421,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the peer may still write its shared memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -428,17 +548,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int kMode>
-cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const Fp8Params& p, int64_t max_tiles,
-                       cudaStream_t st) {
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& ta64, const CUtensorMap& tb, const Fp8Params& p,
+                       int64_t max_units, cudaStream_t st) {
   static PerDeviceOnce attr_once;
   cudaError_t e = attr_once.run([] {
     return cudaFuncSetAttribute(grouped_gemm_fp8_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
   });
   if (e != cudaSuccess) return e;
-  int64_t grid = device_sm_count();
-  if (grid > max_tiles) grid = max_tiles;
-  if (grid < 1) grid = 1;
-  grouped_gemm_fp8_kernel<kMode><<<(unsigned)grid, kThreads, kDynSmem, st>>>(ta, tb, p);
+  // CTA pairs (clusters of two), at most one pair per two SMs
+  int64_t clusters = device_sm_count() / 2;
+  if (clusters > max_units) clusters = max_units;
+  if (clusters < 1) clusters = 1;
+  grouped_gemm_fp8_kernel<kMode><<<(unsigned)(2 * clusters), kThreads, kDynSmem, st>>>(ta, ta64, tb, p);
   return cudaGetLastError();
 }
 
@@ -449,20 +570,25 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                    const void* perm_codes, const void* perm_scales, const void* w13,
                                    const void* w13_scales, const void* w2, const void* w2_scales, void* workspace,
-                                   void* out_fc2, cudaStream_t st) {
+                                   void* out_fc2, int32_t out_format, void* out_fc2_scales, cudaStream_t st) {
   if (l.capacity == 0) return cudaSuccess;
   if (s.E > kMaxE) return cudaErrorNotSupported;
   const uint64_t cap = (uint64_t)l.capacity;
   uint8_t* act = static_cast<uint8_t*>(workspace);
   float* act_scales = reinterpret_cast<float*>(act + round_up(cap * s.I, 1024));
-  CUtensorMap ta1, tb1, ta2, tb2;
+  CUtensorMap ta1, ta1h, tb1, ta2, ta2h, tb2;
   cudaError_t e;
   if ((e = make_tensor_map_2d(&ta1, perm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cap, s.H, BM, BK)) != cudaSuccess)
+    return e;
+  if ((e = make_tensor_map_2d(&ta1h, perm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cap, s.H, BM / 2, BK)) !=
+      cudaSuccess)
     return e;
   if ((e = make_tensor_map_2d(&tb1, w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)s.E * 2 * s.I, s.H, 64, BK)) !=
       cudaSuccess)
     return e;
   if ((e = make_tensor_map_2d(&ta2, act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cap, s.I, BM, BK)) != cudaSuccess) return e;
+  if ((e = make_tensor_map_2d(&ta2h, act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cap, s.I, BM / 2, BK)) != cudaSuccess)
+    return e;
   if ((e = make_tensor_map_2d(&tb2, w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)s.E * s.H, s.I, 128, BK)) !=
       cudaSuccess)
     return e;
@@ -486,7 +612,9 @@ cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, 
   p1.nt = (int)(s.I / 128);
   p1.nkb = (int)(s.H / BK);
   p1.n_blocks_b = (int)(2 * s.I / 128);
-  if ((e = launch_one<kFc1SwiGLU>(ta1, tb1, p1, m_tiles_bound * p1.nt, st)) != cudaSuccess) return e;
+  p1.out_format = MOE_COMBINE_BF16;
+  p1.out_mx_scales = nullptr;
+  if ((e = launch_one<kFc1SwiGLU>(ta1, ta1h, tb1, p1, m_tiles_bound * p1.nt, st)) != cudaSuccess) return e;
   if (prof.after_fc1 && (e = record_profile_event(prof.after_fc1, st)) != cudaSuccess) return e;
 
   Fp8Params p2 = p1;
@@ -501,7 +629,9 @@ cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, 
   p2.nt = (int)((s.H + BN - 1) / BN);
   p2.nkb = (int)(s.I / BK);
   p2.n_blocks_b = (int)(s.H / 128);
-  if ((e = launch_one<kFc2>(ta2, tb2, p2, m_tiles_bound * p2.nt, st)) != cudaSuccess) return e;
+  p2.out_format = out_format;
+  p2.out_mx_scales = static_cast<uint8_t*>(out_fc2_scales);
+  if ((e = launch_one<kFc2>(ta2, ta2h, tb2, p2, m_tiles_bound * p2.nt, st)) != cudaSuccess) return e;
   if (prof.after_fc2 && (e = record_profile_event(prof.after_fc2, st)) != cudaSuccess) return e;
   return cudaSuccess;
 }

@@ -16,7 +16,7 @@ cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shap
 cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                    const void* perm_codes, const void* perm_scales, const void* w13,
                                    const void* w13_scales, const void* w2, const void* w2_scales, void* workspace,
-                                   void* out_fc2, cudaStream_t st);
+                                   void* out_fc2, int32_t out_format, void* out_fc2_scales, cudaStream_t st);
 
 cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                      const void* perm_packed, const void* perm_scales, const void* w13,
@@ -65,8 +65,11 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
                                const void* w13, const void* w13_scales, const void* w2,
                                const void* w2_scales, const moe_nvfp4_globals* globals,
-                               void* workspace, void* out_fc2, cudaStream_t st) {
+                               void* workspace, void* out_fc2, int32_t out_format, void* out_fc2_scales,
+                               cudaStream_t st) {
   const int64_t silent = take_debug_mlp_silent_tile();  // testing hook: only the fused bf16 kernel uses it
+  // MX combine formats are written by the FP8 path's FC2 epilogue only
+  if (out_format != MOE_COMBINE_BF16 && w_dtype != MOE_DTYPE_FP8_E4M3_B128) return cudaErrorNotSupported;
   switch (w_dtype) {
     case MOE_DTYPE_BF16:
       if (grouped_mlp_bf16_uses_pairs(s, l))
@@ -76,7 +79,7 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                      out_fc2, st, silent);
     case MOE_DTYPE_FP8_E4M3_B128:
       return launch_grouped_mlp_fp8(h, s, l, perm_tokens, perm_scales, w13, w13_scales, w2, w2_scales, workspace,
-                                    out_fc2, st);
+                                    out_fc2, out_format, out_fc2_scales, st);
     case MOE_DTYPE_NVFP4:
       return launch_grouped_mlp_nvfp4(h, s, l, perm_tokens, perm_scales, w13, w13_scales, w2, w2_scales, *globals,
                                       workspace, out_fc2, st);

@@ -146,6 +146,19 @@ moe_status moe_capacity(int64_t rows, double factor, int64_t align, int64_t* cap
   return MOE_OK;
 }
 
+moe_status moe_decode_bucket(int64_t tokens, const int64_t* ladder, int32_t n, int64_t* bucket_out) {
+  if (!ladder || !bucket_out || n < 1 || tokens < 0) return MOE_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; i++)
+    if (ladder[i] < 1 || (i > 0 && ladder[i] <= ladder[i - 1])) return MOE_ERR_INVALID_ARG;
+  const int64_t want = tokens > 0 ? tokens : 1;  // zero tokens keep the smallest non-empty bucket
+  for (int32_t i = 0; i < n; i++)
+    if (ladder[i] >= want) {
+      *bucket_out = ladder[i];
+      return MOE_OK;
+    }
+  return MOE_ERR_INVALID_ARG;  // above the largest bucket
+}
+
 moe_status moe_routing_map_bytes(int32_t format, int64_t T, int64_t E, int64_t K, size_t* bytes_out) {
   if (!bytes_out || T < 0 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (format == MOE_ROUTING_SPARSE_BOOL)
@@ -242,6 +255,34 @@ moe_status moe_combine_unpermute(const moe_handle_dev* handle, const moe_shape* 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+moe_status moe_combine_unpermute_fmt(const moe_handle_dev* handle, const moe_shape* shape,
+                                     const moe_layout* layout, int32_t in_format, const void* expert_out,
+                                     const void* expert_out_scales, const float* perm_probs, void* y,
+                                     void* stream) {
+  if (in_format == MOE_COMBINE_BF16)
+    return moe_combine_unpermute(handle, shape, layout, expert_out, perm_probs, y, stream);
+  if (in_format != MOE_COMBINE_MXFP8 && in_format != MOE_COMBINE_MXFP4) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_handle(handle));
+  MOE_TRY(check_shape(shape, true));
+  MOE_TRY(check_layout(layout));
+  MOE_TRY(check_padded_total(shape, layout));
+  if (!expert_out || !expert_out_scales || (shape->T > 0 && !y) || !aligned16(expert_out) || !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_combine_mx(*handle, *shape, in_format, expert_out, expert_out_scales, perm_probs, y,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status moe_quantize_mx_rows(const void* x, int64_t R, int64_t H, int32_t format, void* codes, void* scales,
+                                void* stream) {
+  if (R < 0 || H <= 0 || H % 32 || (format != MOE_COMBINE_MXFP8 && format != MOE_COMBINE_MXFP4))
+    return MOE_ERR_INVALID_ARG;
+  if (R == 0) return MOE_OK;
+  if (!x || !codes || !scales || !aligned16(x) || !aligned16(codes)) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_quantize_mx_rows(x, R, H, format, codes, scales, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
 moe_status moe_combine_backward(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
                                 const void* grad_y, const void* expert_out, const float* perm_probs,
                                 void* grad_expert_out, float* grad_perm_probs, void* stream) {
@@ -304,6 +345,21 @@ moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape,
                            const void* w13, const void* w13_scales, const void* w2,
                            const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
                            size_t workspace_bytes, void* out_fc2, void* stream) {
+  return moe_grouped_mlp_fmt(handle, shape, layout, w_dtype, perm_tokens, perm_scales, w13, w13_scales, w2,
+                             w2_scales, globals, workspace, workspace_bytes, MOE_COMBINE_BF16, out_fc2, nullptr,
+                             stream);
+}
+
+moe_status moe_grouped_mlp_fmt(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
+                               int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
+                               const void* w13, const void* w13_scales, const void* w2,
+                               const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
+                               size_t workspace_bytes, int32_t out_format, void* out_fc2, void* out_fc2_scales,
+                               void* stream) {
+  if (out_format != MOE_COMBINE_BF16 && out_format != MOE_COMBINE_MXFP8 && out_format != MOE_COMBINE_MXFP4)
+    return MOE_ERR_INVALID_ARG;
+  if (out_format != MOE_COMBINE_BF16 && (!out_fc2_scales || (reinterpret_cast<uintptr_t>(out_fc2_scales) & 3u)))
+    return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_handle(handle));
   MOE_TRY(check_shape(shape, true));
   MOE_TRY(check_layout(layout));
@@ -329,8 +385,8 @@ moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape,
   }
   if (workspace_bytes < grouped_mlp_workspace_bytes(*shape, *layout, w_dtype)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaError_t e = launch_grouped_mlp(*handle, *shape, *layout, w_dtype, perm_tokens, perm_scales, w13,
-                                     w13_scales, w2, w2_scales, globals, workspace, out_fc2,
-                                     static_cast<cudaStream_t>(stream));
+                                     w13_scales, w2, w2_scales, globals, workspace, out_fc2, out_format,
+                                     out_fc2_scales, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }

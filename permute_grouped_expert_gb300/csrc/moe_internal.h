@@ -75,7 +75,13 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
                                const void* w13, const void* w13_scales, const void* w2,
                                const void* w2_scales, const moe_nvfp4_globals* globals,
-                               void* workspace, void* out_fc2, cudaStream_t st);
+                               void* workspace, void* out_fc2, int32_t out_format, void* out_fc2_scales,
+                               cudaStream_t st);
+cudaError_t launch_combine_mx(const moe_handle_dev& h, const moe_shape& s, int32_t in_format,
+                              const void* codes, const void* scales, const float* perm_probs, void* y,
+                              cudaStream_t st);
+cudaError_t launch_quantize_mx_rows(const void* x, int64_t R, int64_t H, int32_t format, void* codes, void* scales,
+                                    cudaStream_t st);
 
 int device_sm_count();
 

@@ -12,6 +12,8 @@
 // (TopkReduce combine; NVFP4 block scales with a global scale).
 #include <algorithm>
 
+#include <cuda_fp16.h>
+
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -356,6 +358,189 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineParams p) {
   }
 }
 
+// ---------------------------------------------------------- MX combine formats
+// E4M3 (MXFP8) or E2M1 (MXFP4) elements with one E8M0 scale 2^X per 32: X =
+// floor(log2(amax)) - emax (8 for E4M3, 2 for E2M1) clamped to [-127, 127], 0
+// for an all-zero block; element = x / 2^X rounded to nearest even, saturating.
+
+// 2^(code - 127) for an E8M0 code in [0, 254] (code 0 is the fp32 subnormal 2^-127).
+__device__ __forceinline__ float e8m0_to_float(uint32_t code) {
+  return code ? __uint_as_float(code << 23) : __uint_as_float(0x00400000u);
+}
+
+// Shared exponent X of a block with magnitude maximum amax (exact, from the fp32 bits).
+__device__ __forceinline__ int mx_exponent(float amax, int emax) {
+  if (amax == 0.0f) return 0;
+  const int field = (int)((__float_as_uint(amax) >> 23) & 0xff);  // 0 for a subnormal: floor(log2) <= -127
+  const int X = (field == 0 ? -127 : field - 127) - emax;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
+// Two E4M3 codes (low byte first) -> two floats.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t pair) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(pair));
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// Two E2M1 codes in one byte (low nibble first) -> two floats.
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(byte));
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+struct CombineMxParams {
+  int64_t T, H, K;
+  int64_t nchunks, chunk_steps;  // work items per token; 64-group steps per item
+  const int32_t* row_of;
+  const uint8_t* codes;   // E4M3 [cap][H] or packed E2M1 [cap][H/2]
+  const uint8_t* scales;  // E8M0 [cap][H/32]
+  const float* perm_probs;
+  uint8_t* y;
+};
+
+// y[t] = bf16(sum_k w_k * decoded O[row_k]), fp32 accumulation in ascending k,
+// a lane handling 16 consecutive elements (one half of an MX block) per group.
+template <int kElem>
+__global__ void __launch_bounds__(kThreads) combine_mx_kernel(CombineMxParams p) {
+  __shared__ int32_t s_row[kWarps][kMaxK];
+  __shared__ float s_w[kWarps][kMaxK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t ngroups = p.H / 16;
+  const int64_t row_bytes = kElem == 0 ? p.H : p.H / 2;
+  const int64_t nsc = p.H / 32;
+  const int64_t items = p.T * p.nchunks;
+  for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
+    const int64_t t = it / p.nchunks, chunk = it - t * p.nchunks;
+    int nk = 0;
+    for (int k0 = 0; k0 < p.K; k0 += 32) {
+      const int k = k0 + lane;
+      int32_t r = (k < p.K) ? p.row_of[t * p.K + k] : -1;
+      const unsigned keep = __ballot_sync(0xffffffffu, r >= 0);
+      if (r >= 0) {
+        const int slot = nk + __popc(keep & lanemask_lt());
+        s_row[warp][slot] = r;
+        s_w[warp][slot] = p.perm_probs ? p.perm_probs[r] : 1.0f;
+      }
+      nk += __popc(keep);
+    }
+    __syncwarp();
+    const int64_t gend = min64(ngroups, (chunk + 1) * p.chunk_steps * 64);
+    for (int64_t base = chunk * p.chunk_steps * 64; base < gend; base += 64) {
+      float acc[2][16];
+#pragma unroll
+      for (int u = 0; u < 2; u++)
+#pragma unroll
+        for (int j = 0; j < 16; j++) acc[u][j] = 0.0f;
+      for (int k0 = 0; k0 < nk; k0 += 4) {
+        uint4 v[4][2];
+        float sc[4][2];
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++) {
+          if (k0 + kk < nk) {
+            const int64_t r = s_row[warp][k0 + kk];
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+              const int64_t g = base + u * 32 + lane;
+              if (g < gend) {
+                if (kElem == 0) {
+                  v[kk][u] = ld_stream(p.codes + r * row_bytes + g * 16);
+                } else {
+                  const uint2 h = *reinterpret_cast<const uint2*>(p.codes + r * row_bytes + g * 8);
+                  v[kk][u] = make_uint4(h.x, h.y, 0, 0);
+                }
+                sc[kk][u] = e8m0_to_float(__ldg(p.scales + r * nsc + g / 2)) * s_w[warp][k0 + kk];
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++) {
+          if (k0 + kk < nk) {
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+              const float ws = sc[kk][u];
+              if (kElem == 0) {
+                const uint32_t w4[4] = {v[kk][u].x, v[kk][u].y, v[kk][u].z, v[kk][u].w};
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                  const float2 a = e4m3x2_to_float2(w4[q] & 0xffffu), b = e4m3x2_to_float2(w4[q] >> 16);
+                  acc[u][4 * q + 0] = fmaf(ws, a.x, acc[u][4 * q + 0]);
+                  acc[u][4 * q + 1] = fmaf(ws, a.y, acc[u][4 * q + 1]);
+                  acc[u][4 * q + 2] = fmaf(ws, b.x, acc[u][4 * q + 2]);
+                  acc[u][4 * q + 3] = fmaf(ws, b.y, acc[u][4 * q + 3]);
+                }
+              } else {
+                const uint32_t w2[2] = {v[kk][u].x, v[kk][u].y};
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                  const float2 a = e2m1x2_to_float2((w2[q >> 2] >> (8 * (q & 3))) & 0xffu);
+                  acc[u][2 * q + 0] = fmaf(ws, a.x, acc[u][2 * q + 0]);
+                  acc[u][2 * q + 1] = fmaf(ws, a.y, acc[u][2 * q + 1]);
+                }
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; u++) {
+        const int64_t g = base + u * 32 + lane;
+        if (g < gend) {
+          uint32_t o[8];
+#pragma unroll
+          for (int j = 0; j < 8; j++) o[j] = float_to_bf16_bits(acc[u][2 * j]) | (float_to_bf16_bits(acc[u][2 * j + 1]) << 16);
+          uint8_t* dst = p.y + (t * p.H + g * 16) * 2;
+          st_vec(dst, make_uint4(o[0], o[1], o[2], o[3]));
+          st_vec(dst + 16, make_uint4(o[4], o[5], o[6], o[7]));
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// One thread per 32-element block of bf16 rows [R][H] -> MX codes + E8M0 scale.
+template <int kElem>
+__global__ void __launch_bounds__(256) quantize_mx_rows_kernel(const uint8_t* x, int64_t R, int64_t H, uint8_t* codes,
+                                                               uint8_t* scales) {
+  const int64_t nblk = R * (H / 32);
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += (int64_t)gridDim.x * blockDim.x) {
+    float f[32];
+#pragma unroll
+    for (int v = 0; v < 4; v++) {
+      const uint4 q = ld_stream(x + b * 64 + v * 16);
+      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        f[v * 8 + 2 * j] = bf16_bits_to_float(w4[j] & 0xffffu);
+        f[v * 8 + 2 * j + 1] = bf16_bits_to_float(w4[j] >> 16);
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; j++) amax = fmaxf(amax, fabsf(f[j]));
+    const int X = mx_exponent(amax, kElem == 0 ? 8 : 2);
+    const float inv = X < 127 ? __uint_as_float((uint32_t)(127 - X) << 23) : __uint_as_float(0x00400000u);
+    if (kElem == 0) {
+      uint32_t c[16];
+#pragma unroll
+      for (int j = 0; j < 16; j++) c[j] = e4m3x2(f[2 * j] * inv, f[2 * j + 1] * inv);
+      uint8_t* dst = codes + b * 32;
+      st_vec(dst, make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16)));
+      st_vec(dst + 16,
+             make_uint4(c[8] | (c[9] << 16), c[10] | (c[11] << 16), c[12] | (c[13] << 16), c[14] | (c[15] << 16)));
+    } else {
+      uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int j = 0; j < 16; j++) w[j >> 2] |= e2m1x2(f[2 * j] * inv, f[2 * j + 1] * inv) << (8 * (j & 3));
+      st_vec(codes + b * 16, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+    scales[b] = (uint8_t)(X + 127);
+  }
+}
+
 // One CTA per 128x128 block of a bf16 weight [G][N][Kd]: fp32 scale amax/448
 // (1 for an all-zero block) and E4M3 codes of w / scale.
 __global__ void __launch_bounds__(256) quantize_fp8_blocks_kernel(const uint8_t* w, int64_t N,
@@ -537,6 +722,44 @@ cudaError_t launch_combine(const moe_handle_dev& h, const moe_shape& s, const mo
   p.y = static_cast<uint8_t*>(y);
   row_split(s.T, (s.H / 8 + 63) / 64, &p.nchunks, &p.chunk_steps);
   combine_kernel<<<grid_for(s.T * p.nchunks), kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_mx(const moe_handle_dev& h, const moe_shape& s, int32_t in_format,
+                              const void* codes, const void* scales, const float* perm_probs, void* y,
+                              cudaStream_t st) {
+  CombineMxParams p;
+  p.T = s.T;
+  p.H = s.H;
+  p.K = s.K;
+  p.row_of = h.row_of;
+  p.codes = static_cast<const uint8_t*>(codes);
+  p.scales = static_cast<const uint8_t*>(scales);
+  p.perm_probs = perm_probs;
+  p.y = static_cast<uint8_t*>(y);
+  row_split(s.T, (s.H / 16 + 63) / 64, &p.nchunks, &p.chunk_steps);
+  if (in_format == MOE_COMBINE_MXFP8)
+    combine_mx_kernel<0><<<grid_for(s.T * p.nchunks), kThreads, 0, st>>>(p);
+  else
+    combine_mx_kernel<1><<<grid_for(s.T * p.nchunks), kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mx_rows(const void* x, int64_t R, int64_t H, int32_t format, void* codes, void* scales,
+                                    cudaStream_t st) {
+  const int64_t nblk = R * (H / 32);
+  int64_t blocks = (nblk + 255) / 256;
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (format == MOE_COMBINE_MXFP8)
+    quantize_mx_rows_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint8_t*>(x), R, H,
+                                                                 static_cast<uint8_t*>(codes),
+                                                                 static_cast<uint8_t*>(scales));
+  else
+    quantize_mx_rows_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint8_t*>(x), R, H,
+                                                                 static_cast<uint8_t*>(codes),
+                                                                 static_cast<uint8_t*>(scales));
   return cudaGetLastError();
 }
 

@@ -164,6 +164,38 @@ MOE_DEVICE void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 namespace moe {
 namespace sm100 {
 
+// ------------------------------------------------------ clusters of CTAs
+// Helpers for kernels whose CTAs, each driving its own tensor cores
+// (cta_group::1), share operand tiles with a peer of their cluster.
+
+// 2-D tiled load written to the same shared-memory offset in every CTA of
+// `mask` (this GPU's own memory only); each destination CTA's mbarrier at
+// `bar`'s offset receives the transaction bytes.
+MOE_DEVICE void tma_load_2d_mc(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1, uint64_t* bar,
+                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once every
+// MMA this thread issued so far (cta_group::1) has completed.
+MOE_DEVICE void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+}  // namespace sm100
+}  // namespace moe
+
+namespace moe {
+namespace sm100 {
+
 // ------------------------------------------------------------ CTA pairs
 // Helpers for kernels launched with clusters of two CTAs that drive the
 // tensor cores of both SMs with one MMA (cta_group::2).

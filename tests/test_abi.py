@@ -215,3 +215,21 @@ def test_debug_hook_arguments(moe):
     moe.moe_debug_next_grouped_mlp_silent_token_tile(-1)
     with pytest.raises(moe.MoeError):
         moe.moe_debug_next_grouped_mlp_silent_token_tile(-2)
+
+
+def test_decode_bucket_selection(moe):
+    """Smallest bucket that holds the batch; zero tokens keep the smallest
+    bucket (a non-empty launch); above the largest bucket, or a malformed
+    ladder, is an argument error."""
+    ladder = [1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192]
+    assert moe.moe_decode_bucket(0, ladder) == 1
+    assert moe.moe_decode_bucket(1, ladder) == 1
+    assert moe.moe_decode_bucket(37, ladder) == 64
+    assert moe.moe_decode_bucket(64, ladder) == 64
+    assert moe.moe_decode_bucket(65, ladder) == 128
+    assert moe.moe_decode_bucket(8192, ladder) == 8192
+    assert moe.moe_decode_bucket(100, [64, 256, 8192]) == 256
+    for bad in ((8193, ladder), (-1, ladder), (5, []), (5, [4, 4, 8]), (5, [8, 4]), (5, [0, 4])):
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_decode_bucket(*bad)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG

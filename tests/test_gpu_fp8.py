@@ -112,7 +112,7 @@ def test_dsv3_layer_full_size_sampled(oracle, moe):
     toks = np.sort(np.random.default_rng(3).choice(w.T, 6, replace=False))
     tok_rows = np.unique(pre["row_of"][toks][pre["row_of"][toks] >= 0])
     head_rows, head = largest_expert_rows(pre, r["cap"], 128)
-    assert pre["counts"][head] > 60 * 128  # the Zipf head spans dozens of token tiles
+    assert pre["counts"][head] > 50 * 128  # the Zipf head spans dozens of token tiles
     edge_rows = segment_edge_rows(pre, r["cap"])
     assert len(edge_rows) >= 2 * 250
     rows = np.unique(np.concatenate([tok_rows, head_rows, edge_rows]))
