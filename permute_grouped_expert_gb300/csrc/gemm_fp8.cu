@@ -16,7 +16,14 @@
 // partial into fp32 register accumulators with the product of the row's and
 // the weight block's scales while the tensor cores fill the other buffer.
 //
-// One CTA per SM, 10 warps:
+// CTA pairs (clusters of two, one CTA per SM).  A pair takes two tiles that
+// share an operand: two token tiles of one expert with the same weight tile,
+// or, for an expert's last odd token tile, two output tiles of that token
+// tile.  Each CTA loads its own operand and half of the shared one, which TMA
+// multicasts into both CTAs' shared memory, so the pair reads the shared tile
+// from L2 once; each CTA's MMA commit releases a stage in both CTAs.
+//
+// 10 warps per CTA:
 //   warp 0      TMA producer (A 128 x 128 B, B 256 x 128 B per stage, 4 stages)
 //   warp 1      TMEM allocation (512 columns = 2 partials of 128 x 256 fp32) and
 //               MMA issue from one thread
@@ -27,7 +34,8 @@
 //               spill accumulators to local memory inside the K loop).
 // FC1's weight tile interleaves up and gate rows in 64-row boxes so that each
 // thread ends a tile holding the up and gate values of the same 64 output
-// columns.  Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit).
+// columns.  Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit of
+// both CTAs).
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
 #include "tensor_map.h"

@@ -392,7 +392,7 @@ __device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
 
 struct CombineMxParams {
   int64_t T, H, K;
-  int64_t nchunks, chunk_steps;  // work items per token; 64-group steps per item
+  int64_t nchunks, chunk_steps;  // work items per token; loop steps per item
   const int32_t* row_of;
   const uint8_t* codes;   // E4M3 [cap][H] or packed E2M1 [cap][H/2]
   const uint8_t* scales;  // E8M0 [cap][H/32]
@@ -400,16 +400,19 @@ struct CombineMxParams {
   uint8_t* y;
 };
 
-// y[t] = bf16(sum_k w_k * decoded O[row_k]), fp32 accumulation in ascending k,
-// a lane handling 16 consecutive elements (one half of an MX block) per group.
+// y[t] = bf16(sum_k w_k * decoded O[row_k]), fp32 accumulation in ascending k.
+// A lane handles one MX block (32 consecutive elements, one scale byte) per
+// step and loads it for up to 8 routes at once: 8 x 32 bytes in flight per lane
+// for MXFP8, 8 x 16 for MXFP4.
 template <int kElem>
-__global__ void __launch_bounds__(kThreads) combine_mx_kernel(CombineMxParams p) {
+__global__ void __launch_bounds__(kThreads, 2) combine_mx_kernel(CombineMxParams p) {
   __shared__ int32_t s_row[kWarps][kMaxK];
   __shared__ float s_w[kWarps][kMaxK];
+  constexpr int kKC = 8;                       // routes loaded together
+  constexpr int kVec = kElem == 0 ? 2 : 1;     // 16-byte vectors per block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t ngroups = p.H / 16;
+  const int64_t nblk = p.H / 32;
   const int64_t row_bytes = kElem == 0 ? p.H : p.H / 2;
-  const int64_t nsc = p.H / 32;
   const int64_t items = p.T * p.nchunks;
   for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
     const int64_t t = it / p.nchunks, chunk = it - t * p.nchunks;
@@ -426,75 +429,61 @@ __global__ void __launch_bounds__(kThreads) combine_mx_kernel(CombineMxParams p)
       nk += __popc(keep);
     }
     __syncwarp();
-    const int64_t gend = min64(ngroups, (chunk + 1) * p.chunk_steps * 64);
-    for (int64_t base = chunk * p.chunk_steps * 64; base < gend; base += 64) {
-      float acc[2][16];
+    const int64_t bend = min64(nblk, (chunk + 1) * p.chunk_steps * 32);
+    for (int64_t b = chunk * p.chunk_steps * 32 + lane; b < bend; b += 32) {
+      float acc[32];
 #pragma unroll
-      for (int u = 0; u < 2; u++)
+      for (int j = 0; j < 32; j++) acc[j] = 0.0f;
+      for (int k0 = 0; k0 < nk; k0 += kKC) {
+        uint4 v[kKC][kVec];
+        uint32_t sc[kKC];
 #pragma unroll
-        for (int j = 0; j < 16; j++) acc[u][j] = 0.0f;
-      for (int k0 = 0; k0 < nk; k0 += 4) {
-        uint4 v[4][2];
-        float sc[4][2];
-#pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
+        for (int kk = 0; kk < kKC; kk++) {
           if (k0 + kk < nk) {
             const int64_t r = s_row[warp][k0 + kk];
 #pragma unroll
-            for (int u = 0; u < 2; u++) {
-              const int64_t g = base + u * 32 + lane;
-              if (g < gend) {
-                if (kElem == 0) {
-                  v[kk][u] = ld_stream(p.codes + r * row_bytes + g * 16);
-                } else {
-                  const uint2 h = *reinterpret_cast<const uint2*>(p.codes + r * row_bytes + g * 8);
-                  v[kk][u] = make_uint4(h.x, h.y, 0, 0);
-                }
-                sc[kk][u] = e8m0_to_float(__ldg(p.scales + r * nsc + g / 2)) * s_w[warp][k0 + kk];
-              }
-            }
+            for (int q = 0; q < kVec; q++) v[kk][q] = ld_stream(p.codes + r * row_bytes + b * 16 * kVec + 16 * q);
+            sc[kk] = __ldg(p.scales + r * nblk + b);
           }
         }
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
+        for (int kk = 0; kk < kKC; kk++) {
           if (k0 + kk < nk) {
+            const float ws = e8m0_to_float(sc[kk]) * s_w[warp][k0 + kk];
+            if (kElem == 0) {
 #pragma unroll
-            for (int u = 0; u < 2; u++) {
-              const float ws = sc[kk][u];
-              if (kElem == 0) {
-                const uint32_t w4[4] = {v[kk][u].x, v[kk][u].y, v[kk][u].z, v[kk][u].w};
+              for (int q = 0; q < 2; q++) {
+                const uint32_t w4[4] = {v[kk][q].x, v[kk][q].y, v[kk][q].z, v[kk][q].w};
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                  const float2 a = e4m3x2_to_float2(w4[q] & 0xffffu), b = e4m3x2_to_float2(w4[q] >> 16);
-                  acc[u][4 * q + 0] = fmaf(ws, a.x, acc[u][4 * q + 0]);
-                  acc[u][4 * q + 1] = fmaf(ws, a.y, acc[u][4 * q + 1]);
-                  acc[u][4 * q + 2] = fmaf(ws, b.x, acc[u][4 * q + 2]);
-                  acc[u][4 * q + 3] = fmaf(ws, b.y, acc[u][4 * q + 3]);
+                for (int i = 0; i < 4; i++) {
+                  const float2 a = e4m3x2_to_float2(w4[i] & 0xffffu), c = e4m3x2_to_float2(w4[i] >> 16);
+                  float* d = acc + 16 * q + 4 * i;
+                  d[0] = fmaf(ws, a.x, d[0]);
+                  d[1] = fmaf(ws, a.y, d[1]);
+                  d[2] = fmaf(ws, c.x, d[2]);
+                  d[3] = fmaf(ws, c.y, d[3]);
                 }
-              } else {
-                const uint32_t w2[2] = {v[kk][u].x, v[kk][u].y};
+              }
+            } else {
+              const uint32_t w4[4] = {v[kk][0].x, v[kk][0].y, v[kk][0].z, v[kk][0].w};
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
-                  const float2 a = e2m1x2_to_float2((w2[q >> 2] >> (8 * (q & 3))) & 0xffu);
-                  acc[u][2 * q + 0] = fmaf(ws, a.x, acc[u][2 * q + 0]);
-                  acc[u][2 * q + 1] = fmaf(ws, a.y, acc[u][2 * q + 1]);
-                }
+              for (int q = 0; q < 16; q++) {
+                const float2 a = e2m1x2_to_float2((w4[q >> 2] >> (8 * (q & 3))) & 0xffu);
+                acc[2 * q] = fmaf(ws, a.x, acc[2 * q]);
+                acc[2 * q + 1] = fmaf(ws, a.y, acc[2 * q + 1]);
               }
             }
           }
         }
       }
+      uint8_t* dst = p.y + (t * p.H + b * 32) * 2;
 #pragma unroll
-      for (int u = 0; u < 2; u++) {
-        const int64_t g = base + u * 32 + lane;
-        if (g < gend) {
-          uint32_t o[8];
+      for (int q = 0; q < 4; q++) {
+        uint32_t o[4];
 #pragma unroll
-          for (int j = 0; j < 8; j++) o[j] = float_to_bf16_bits(acc[u][2 * j]) | (float_to_bf16_bits(acc[u][2 * j + 1]) << 16);
-          uint8_t* dst = p.y + (t * p.H + g * 16) * 2;
-          st_vec(dst, make_uint4(o[0], o[1], o[2], o[3]));
-          st_vec(dst + 16, make_uint4(o[4], o[5], o[6], o[7]));
-        }
+        for (int j = 0; j < 4; j++)
+          o[j] = float_to_bf16_bits(acc[8 * q + 2 * j]) | (float_to_bf16_bits(acc[8 * q + 2 * j + 1]) << 16);
+        st_vec(dst + 16 * q, make_uint4(o[0], o[1], o[2], o[3]));
       }
     }
     __syncwarp();
@@ -737,7 +726,7 @@ cudaError_t launch_combine_mx(const moe_handle_dev& h, const moe_shape& s, int32
   p.scales = static_cast<const uint8_t*>(scales);
   p.perm_probs = perm_probs;
   p.y = static_cast<uint8_t*>(y);
-  row_split(s.T, (s.H / 16 + 63) / 64, &p.nchunks, &p.chunk_steps);
+  row_split(s.T, (s.H / 32 + 31) / 32, &p.nchunks, &p.chunk_steps);
   if (in_format == MOE_COMBINE_MXFP8)
     combine_mx_kernel<0><<<grid_for(s.T * p.nchunks), kThreads, 0, st>>>(p);
   else
