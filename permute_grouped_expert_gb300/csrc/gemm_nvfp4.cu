@@ -43,9 +43,8 @@ using namespace sm100;
 constexpr int BMW = 128;        // weight rows per tile (MMA M)
 constexpr int BNT = 32;         // tokens per tile (MMA N)
 constexpr int BKR = 256;        // K elements per raw stage
-constexpr int BKC = 64;         // K elements per converted stage
+constexpr int BKC = 64;         // K elements per converted slice (one 128-byte swizzle atom of f16)
 constexpr int kRawStages = 4;
-constexpr int kCvtStages = 5;
 constexpr int kCvtWarps = 8;
 constexpr int kThreads = 64 + 32 * kCvtWarps + 128;
 constexpr uint32_t kRawW = BMW * (BKR / 2);        // 16 KB packed weights
@@ -56,10 +55,24 @@ constexpr uint32_t kRawBytes = kRawW + kRawWS + kRawX + kRawXS;
 constexpr uint32_t kRawStride = 23552;             // kRawBytes rounded up to 1024
 constexpr uint32_t kCvtW = BMW * BKC * 2;          // 16 KB
 constexpr uint32_t kCvtX = BNT * BKC * 2;          // 4 KB
-constexpr uint32_t kCvtStride = kCvtW + kCvtX;     // 20 KB
+constexpr uint32_t kCvtSlice = kCvtW + kCvtX;      // 20 KB: one slice, weights then tokens
+// Converted stages.  FC2 hands two slices (128 K) to the tensor cores per stage,
+// one proxy fence and one barrier arrival per 128 K per converter warp (3
+// stages); FC1, which keeps 25 KB of static shared memory for its gate
+// exchange, runs five one-slice stages, which measured faster there than two
+// two-slice stages.
+template <int kMode>
+constexpr int slices_per_cvt() { return kMode == 0 ? 1 : 2; }
+template <int kMode>
+constexpr int cvt_stages() { return kMode == 0 ? 5 : 3; }
+template <int kMode>
+constexpr uint32_t cvt_stride() { return slices_per_cvt<kMode>() * kCvtSlice; }
 constexpr uint32_t kTmemCols = 64;
 constexpr int kMaxE = 1024;
-constexpr size_t kDynSmem = 1024 + (size_t)kRawStages * kRawStride + (size_t)kCvtStages * kCvtStride;
+template <int kMode>
+constexpr size_t dyn_smem() {
+  return 1024 + (size_t)kRawStages * kRawStride + (size_t)cvt_stages<kMode>() * cvt_stride<kMode>();
+}
 static_assert(kRawBytes <= kRawStride, "raw stage layout");
 
 enum Mode { kFc1SwiGLU = 0, kFc2 = 1 };
@@ -169,6 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                               const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xs,
                               Fp4Params p) {
   extern __shared__ uint8_t dyn_smem[];
+  constexpr int kCvtStages = cvt_stages<kMode>();
+  constexpr int kSlicesPerCvt = slices_per_cvt<kMode>();
+  constexpr uint32_t kCvtStride = cvt_stride<kMode>();
   __shared__ __align__(8) uint64_t s_rfull[kRawStages], s_rempty[kRawStages], s_cfull[kCvtStages],
       s_cempty[kCvtStages], s_tfull[2], s_tempty[2], s_xbar[2], s_drain;
   __shared__ uint32_t s_tmem;
@@ -297,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cst = 0, acc = 0;
       uint32_t cphase = 0, acc_phase = 0;
       bool ok = true;
-      const int nsub = p.nkr * (BKR / BKC);
+      const int nsub = p.nkr * (BKR / BKC) / kSlicesPerCvt;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         if (!mbar_wait(&s_tempty[acc], acc_phase ^ 1, abort_flag, p.status)) {
           ok = false;
@@ -311,12 +327,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t cw = smem_u32(cvt + (size_t)cst * kCvtStride);
-          const uint64_t wdesc = smem_desc_sw128(cw);
-          const uint64_t xdesc = smem_desc_sw128(cw + kCvtW);
 #pragma unroll
-          for (int k = 0; k < BKC / 16; k++)
-            mma_bf16(d_tmem, wdesc + 2 * k, xdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+          for (int sl = 0; sl < kSlicesPerCvt; sl++) {
+            const uint32_t cw = smem_u32(cvt + (size_t)cst * kCvtStride + (size_t)sl * kCvtSlice);
+            const uint64_t wdesc = smem_desc_sw128(cw);
+            const uint64_t xdesc = smem_desc_sw128(cw + kCvtW);
+#pragma unroll
+            for (int k = 0; k < BKC / 16; k++)
+              mma_bf16(d_tmem, wdesc + 2 * k, xdesc + 2 * k, idesc, (ks | sl | k) != 0 ? 1u : 0u);
+          }
           mma_commit(&s_cempty[cst]);
           if (++cst == kCvtStages) {
             cst = 0;
@@ -361,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint8_t* st = raw + (size_t)rst * kRawStride;
-        for (int s = 0; s < BKR / BKC; s++) {
+        for (int s0 = 0; s0 < BKR / BKC; s0 += kSlicesPerCvt) {
           int c_ok = 0;
           if (lane == 0) c_ok = mbar_wait(&s_cempty[cst], cphase ^ 1, abort_flag, p.status) ? 1 : 0;
           c_ok = __shfl_sync(0xffffffffu, c_ok, 0);
@@ -369,12 +388,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          uint8_t* cs = cvt + (size_t)cst * kCvtStride;
-          convert_half_row(st + wrow * (BKR / 2), wrow, s, whalf, st + kRawW + wrow * (BKR / 16),
-                           cs + wrow * (BKC * 2));
-          if (x_conv)
-            convert_half_row(st + kRawW + kRawWS + xrow * (BKR / 2), xrow, s, xhalf,
-                             st + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2));
+#pragma unroll
+          for (int sl = 0; sl < kSlicesPerCvt; sl++) {
+            const int s = s0 + sl;
+            uint8_t* cs = cvt + (size_t)cst * kCvtStride + (size_t)sl * kCvtSlice;
+            convert_half_row(st + wrow * (BKR / 2), wrow, s, whalf, st + kRawW + wrow * (BKR / 16),
+                             cs + wrow * (BKC * 2));
+            if (x_conv)
+              convert_half_row(st + kRawW + kRawWS + xrow * (BKR / 2), xrow, s, xhalf,
+                               st + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2));
+          }
           // make the generic-proxy stores visible to the tensor cores, then publish
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
@@ -480,13 +503,14 @@ cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tws, const CUte
                        const Fp4Params& p, int64_t max_tiles, cudaStream_t st) {
   static PerDeviceOnce attr_once;
   cudaError_t e = attr_once.run([] {
-    return cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+    return cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)dyn_smem<kMode>());
   });
   if (e != cudaSuccess) return e;
   int64_t grid = device_sm_count();
   if (grid > max_tiles) grid = max_tiles;
   if (grid < 1) grid = 1;
-  grouped_gemm_nvfp4_kernel<kMode><<<(unsigned)grid, kThreads, kDynSmem, st>>>(tw, tws, tx, txs, p);
+  grouped_gemm_nvfp4_kernel<kMode><<<(unsigned)grid, kThreads, dyn_smem<kMode>(), st>>>(tw, tws, tx, txs, p);
   return cudaGetLastError();
 }
 
