@@ -176,6 +176,66 @@ __device__ __forceinline__ void convert_half_row(const uint8_t* raw_row_base, in
   }
 }
 
+MOE_DEVICE uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+MOE_DEVICE uint32_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+MOE_DEVICE void sts128(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Where one thread's half row of a 64-element K slice lives, as shared-memory
+// byte offsets fixed for the whole kernel: the row's 128-byte swizzle permutes
+// 16-byte chunks by row & 7, so the input chunk of slice s and the four output
+// chunks of the half are precomputed once.
+struct HalfRow {
+  uint32_t in_off[BKR / BKC];  // raw 16-byte chunk of slice s (half h) within the row
+  uint32_t out_off[4];         // converted chunks 4h .. 4h+3 within the row
+  uint32_t scale_off;          // this half's two scale bytes within a slice's four
+};
+
+__device__ __forceinline__ HalfRow half_row(int r, int h) {
+  HalfRow hr;
+  const int sw = r & 7;
+#pragma unroll
+  for (int s = 0; s < BKR / BKC; s++) hr.in_off[s] = (uint32_t)(((2 * s + h) ^ sw) << 4);
+#pragma unroll
+  for (int j = 0; j < 4; j++) hr.out_off[j] = (uint32_t)(((4 * h + j) ^ sw) << 4);
+  hr.scale_off = (uint32_t)(2 * h);
+  return hr;
+}
+
+// convert_half_row with 32-bit shared-memory addresses and precomputed swizzle
+// offsets (the form FC2 measured faster with; FC1 measured slower with it).
+__device__ __forceinline__ void convert_half_row_sh(uint32_t raw_row, uint32_t scales_row, uint32_t cvt_row, int s,
+                                                    const HalfRow& hr) {
+  const uint4 c = lds128(raw_row + hr.in_off[s]);
+  const uint32_t sc2 = lds16(scales_row + 4 * s + hr.scale_off);
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int g = 0; g < 2; g++) {
+    const uint32_t sh = e4m3_pair_to_f16x2((sc2 >> (8 * g)) & 0xffu);
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+      uint4 o = e2m1x8_to_f16x8(words[2 * g + i]);
+      o.x = hmul2(o.x, sh);
+      o.y = hmul2(o.y, sh);
+      o.z = hmul2(o.z, sh);
+      o.w = hmul2(o.w, sh);
+      sts128(cvt_row + hr.out_off[2 * g + i], o);
+    }
+  }
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
@@ -361,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c = threadIdx.x - 64;  // 0..255: weight row c & 127, half c >> 7
     const int wrow = c & 127, whalf = c >> 7;
     const int xrow = c >> 1, xhalf = c & 1;  // token half-rows for c < 64: rows 0..15 in warp 2
+    const HalfRow whr = half_row(wrow, whalf), xhr = half_row(xrow, xhalf);
+    const uint32_t raw_base = smem_u32(raw), cvt_base = smem_u32(cvt);
     int rst = 0, cst = 0;
     uint32_t rphase = 0, cphase = 0;
     bool ok = true;
@@ -391,12 +453,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int sl = 0; sl < kSlicesPerCvt; sl++) {
             const int s = s0 + sl;
-            uint8_t* cs = cvt + (size_t)cst * kCvtStride + (size_t)sl * kCvtSlice;
-            convert_half_row(st + wrow * (BKR / 2), wrow, s, whalf, st + kRawW + wrow * (BKR / 16),
-                             cs + wrow * (BKC * 2));
-            if (x_conv)
-              convert_half_row(st + kRawW + kRawWS + xrow * (BKR / 2), xrow, s, xhalf,
-                               st + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2));
+            if (kMode == kFc2) {
+              const uint32_t sts = raw_base + (uint32_t)rst * kRawStride;
+              const uint32_t cs = cvt_base + (uint32_t)cst * kCvtStride + (uint32_t)sl * kCvtSlice;
+              convert_half_row_sh(sts + wrow * (BKR / 2), sts + kRawW + wrow * (BKR / 16), cs + wrow * (BKC * 2), s,
+                                  whr);
+              if (x_conv)
+                convert_half_row_sh(sts + kRawW + kRawWS + xrow * (BKR / 2),
+                                    sts + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2),
+                                    s, xhr);
+            } else {
+              uint8_t* cs = cvt + (size_t)cst * kCvtStride + (size_t)sl * kCvtSlice;
+              convert_half_row(st + wrow * (BKR / 2), wrow, s, whalf, st + kRawW + wrow * (BKR / 16),
+                               cs + wrow * (BKC * 2));
+              if (x_conv)
+                convert_half_row(st + kRawW + kRawWS + xrow * (BKR / 2), xrow, s, xhalf,
+                                 st + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2));
+            }
           }
           // make the generic-proxy stores visible to the tensor cores, then publish
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -427,7 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x, tile_iter++) {
       const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
       int ok = 0;
-      if (lane == 0) ok = mbar_wait(&s_tfull[acc], acc_phase, abort_flag, p.status) ? 1 : 0;
+      // FC2: a tile's whole K loop passes before its accumulator is full; poll
+      // rarely so that the converter warps sharing the schedulers get the issue
+      // slots (FC1 measured slower with it)
+      if (lane == 0)
+        ok = (kMode == kFc2 ? mbar_wait_sleep(&s_tfull[acc], acc_phase, abort_flag, p.status, 256)
+                            : mbar_wait(&s_tfull[acc], acc_phase, abort_flag, p.status))
+                 ? 1
+                 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();

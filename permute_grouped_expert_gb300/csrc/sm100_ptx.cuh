@@ -64,6 +64,24 @@ MOE_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, i
   }
 }
 
+// mbar_wait for long waits: sleeps `sleep_ns` between polls instead of spinning,
+// leaving the issue slots to the warps doing work.  Same bound and abort rules.
+MOE_DEVICE bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status,
+                                uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      set_status(status, MOE_DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ----------------------------------------------------------------------- TMA
 
 MOE_DEVICE void tma_prefetch_desc(const CUtensorMap* map) {
