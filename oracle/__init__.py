@@ -66,7 +66,8 @@ def _load():
             _lib.moe_oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
             _lib.moe_oracle_grouped_mlp_rows.argtypes = (
                 [ctypes.c_int] + [ctypes.c_void_p] * 2 + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 7
-                + [ctypes.c_double] * 2 + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p])
+                + [ctypes.c_double] * 2 + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p])
             _lib.moe_oracle_layer_per_token.argtypes = (
                 [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int64] * 3
                 + [ctypes.c_void_p] * 2 + [ctypes.c_int64] * 2 + [ctypes.c_void_p] * 6 + [ctypes.c_double] * 2
@@ -208,8 +209,9 @@ def quantize_nvfp4_rows(x_bf16: np.ndarray, global_scale: float):
 
 def grouped_mlp_rows(fmt: int, y, y_scales, H: int, I: int, E: int, offsets, w13, w13_scales, w2,
                      w2_scales, rows, w13_global=None, w2_global=None, fc1_in_global: float = 0.0,
-                     fc2_in_global: float = 0.0, want_act: bool = False):
-    """FFN of the listed permuted rows.  Returns (out bf16 [n, H], act float64 [n, I] or None)."""
+                     fc2_in_global: float = 0.0, want_act: bool = False, row_probs=None):
+    """FFN of the listed permuted rows.  Returns (out bf16 [n, H], act float64 [n, I] or None).
+    row_probs ([n]): probabilities applied to the FC2 rows inside the MLP."""
     lib = _load()
     dt = np.uint16 if fmt == FMT_BF16 else np.uint8
     sdt = np.float32 if fmt == FMT_FP8 else np.uint8
@@ -223,9 +225,10 @@ def grouped_mlp_rows(fmt: int, y, y_scales, H: int, I: int, E: int, offsets, w13
     out = np.empty((len(rows), H), np.uint16)
     act = np.empty((len(rows), I), np.float64) if want_act else None
     off = _c(offsets, np.int32)
+    rp = _c(row_probs, np.float32)
     rc = lib.moe_oracle_grouped_mlp_rows(
         fmt, _p(yv), _p(ys), H, I, E, _p(off), _p(w13v), _p(w13s), _p(g13), _p(w2v), _p(w2s), _p(g2),
-        fc1_in_global, fc2_in_global, _p(rows), len(rows), _p(out), _p(act))
+        fc1_in_global, fc2_in_global, _p(rows), len(rows), _p(out), _p(act), _p(rp))
     if rc != 0:
         raise ValueError("a listed row lies in no expert segment")
     return out, act
@@ -265,7 +268,7 @@ def mx_decode_rows(codes: np.ndarray, scales: np.ndarray, elem: int) -> np.ndarr
 
 def grouped_mlp_rows_mx(fmt: int, y, y_scales, H: int, I: int, E: int, offsets, w13, w13_scales, w2,
                         w2_scales, rows, elem: int, w13_global=None, w2_global=None, fc1_in_global: float = 0.0,
-                        fc2_in_global: float = 0.0):
+                        fc2_in_global: float = 0.0, row_probs=None):
     """FFN of the listed rows with FC2 written in an MX combine format: (codes, E8M0 scales)."""
     lib = _load()
     dt = np.uint16 if fmt == FMT_BF16 else np.uint8
@@ -283,9 +286,10 @@ def grouped_mlp_rows_mx(fmt: int, y, y_scales, H: int, I: int, E: int, offsets, 
     fn = lib.moe_oracle_grouped_mlp_rows_mx
     fn.argtypes = ([ctypes.c_int] + [ctypes.c_void_p] * 2 + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 7
                    + [ctypes.c_double] * 2 + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
-                                              ctypes.c_void_p])
+                                              ctypes.c_void_p, ctypes.c_void_p])
+    rp = _c(row_probs, np.float32)
     rc = fn(fmt, _p(yv), _p(ys), H, I, E, _p(off), _p(w13v), _p(w13s), _p(g13), _p(w2v), _p(w2s), _p(g2),
-            fc1_in_global, fc2_in_global, _p(rows), len(rows), elem, _p(codes), _p(scales))
+            fc1_in_global, fc2_in_global, _p(rows), len(rows), elem, _p(codes), _p(scales), _p(rp))
     if rc != 0:
         raise ValueError("a listed row lies in no expert segment")
     return codes, scales

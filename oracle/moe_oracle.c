@@ -574,6 +574,11 @@ static void ffn_row(const operand* yin, int64_t r, int64_t e, int64_t H, int64_t
  * 2 NVFP4 (y packed [cap][H/2] + e4m3 scales [cap][H/16] with global
  * fc1_in_global; weights packed with e4m3 scales and per-expert globals;
  * the intermediate uses fc2_in_global). */
+/* row_probs (optional, [nrows]): probabilities applied inside the MLP -- each
+ * FC2 row's sums are multiplied by its probability before they are rounded
+ * ([ALLGATHER], Testing: probability gradients flow back through the dispatch,
+ * i.e. the experts consume the dispatched probabilities; the combine then sums
+ * the rows without weights). */
 ORACLE_API int moe_oracle_grouped_mlp_rows(int fmt, const void* y, const void* y_scales,
                                            int64_t H, int64_t I, int64_t E, const int32_t* offsets,
                                            const void* w13, const void* w13_scales,
@@ -581,7 +586,7 @@ ORACLE_API int moe_oracle_grouped_mlp_rows(int fmt, const void* y, const void* y
                                            const void* w2_scales, const float* w2_global,
                                            double fc1_in_global, double fc2_in_global,
                                            const int64_t* rows, int64_t nrows, uint16_t* out,
-                                           double* act_out) {
+                                           double* act_out, const float* row_probs) {
   operand yin = {fmt, y, y_scales, fc1_in_global};
   operand ow13 = {fmt, w13, w13_scales, 0.0};
   operand ow2 = {fmt, w2, w2_scales, 0.0};
@@ -596,7 +601,8 @@ ORACLE_API int moe_oracle_grouped_mlp_rows(int fmt, const void* y, const void* y
     double* acc = (double*)malloc(sizeof(double) * (size_t)H);
     ffn_row(&yin, rows[i], e, H, I, &ow13, w13_global, &ow2, w2_global, fc2_in_global, acc,
             act_out ? act_out + i * I : NULL);
-    for (int64_t n = 0; n < H; n++) out[i * H + n] = moe_oracle_f64_to_bf16(acc[n]);
+    const double pr = row_probs ? (double)row_probs[i] : 1.0;
+    for (int64_t n = 0; n < H; n++) out[i * H + n] = moe_oracle_f64_to_bf16(pr * acc[n]);
     free(acc);
   }
   return bad ? -1 : 0;
@@ -677,7 +683,7 @@ ORACLE_API int moe_oracle_grouped_mlp_rows_mx(int fmt, const void* y, const void
                                               const void* w13_scales, const float* w13_global, const void* w2,
                                               const void* w2_scales, const float* w2_global, double fc1_in_global,
                                               double fc2_in_global, const int64_t* rows, int64_t nrows, int elem,
-                                              uint8_t* out_codes, uint8_t* out_scales) {
+                                              uint8_t* out_codes, uint8_t* out_scales, const float* row_probs) {
   operand yin = {fmt, y, y_scales, fc1_in_global};
   operand ow13 = {fmt, w13, w13_scales, 0.0};
   operand ow2 = {fmt, w2, w2_scales, 0.0};
@@ -692,7 +698,8 @@ ORACLE_API int moe_oracle_grouped_mlp_rows_mx(int fmt, const void* y, const void
     double* acc = (double*)malloc(sizeof(double) * (size_t)H);
     float* accf = (float*)malloc(sizeof(float) * (size_t)H);
     ffn_row(&yin, rows[i], e, H, I, &ow13, w13_global, &ow2, w2_global, fc2_in_global, acc, NULL);
-    for (int64_t n = 0; n < H; n++) accf[n] = f64_to_f32(acc[n]);
+    const double pr = row_probs ? (double)row_probs[i] : 1.0;
+    for (int64_t n = 0; n < H; n++) accf[n] = f64_to_f32(pr * acc[n]);
     moe_oracle_quantize_mx_rows(accf, 1, H, elem, out_codes + i * (elem == 0 ? H : H / 2), out_scales + i * (H / 32));
     free(acc);
     free(accf);
