@@ -147,7 +147,8 @@ def job_throughput(tokens_per_rank: int, world: int, steps: int, ms_slowest: flo
 class Problem:
     """Device-resident inputs, outputs and workspaces of one MoE layer."""
 
-    def __init__(self, moe, w: workloads.Workload, seed: int, dev, combine_format: str = "bf16"):
+    def __init__(self, moe, w: workloads.Workload, seed: int, dev, combine_format: str = "bf16",
+                 probs_in_mlp: bool = False):
         import torch
 
         self.moe, self.w, self.dev = moe, w, dev
@@ -155,6 +156,9 @@ class Problem:
         if self.cfmt != moe.COMBINE_BF16 and w.dtype != "fp8":
             raise SystemExit("--combine-format mxfp8/mxfp4 is written by the FP8 path's FC2 epilogue only")
         self.combine_format = combine_format
+        if probs_in_mlp and w.I == 0:
+            raise SystemExit("--probs-in-mlp needs a workload with an expert MLP")
+        self.probs_in_mlp = probs_in_mlp
         fmt, rmap, probs = workloads.routing_inputs(w, seed)
         self.fmt = fmt
         self.map_host = torch.from_numpy(np.ascontiguousarray(rmap)).pin_memory()
@@ -260,9 +264,9 @@ class Problem:
         if not self.identity:
             if prof:
                 moe.moe_profile_next_grouped_mlp(*prof)
-            moe.moe_grouped_mlp_fmt(self.handle, self.shape, self.layout, self.w_dtype, self.y, self.y_scales,
-                                    self.w13, self.w13_s, self.w2, self.w2_s, self.globals, self.act_ws, self.cfmt,
-                                    self.o, self.o_scales, stream=stream)
+            moe.moe_grouped_mlp_ex(self.handle, self.shape, self.layout, self.w_dtype, self.y, self.y_scales,
+                                   self.w13, self.w13_s, self.w2, self.w2_s, self.globals, self.act_ws, self.cfmt,
+                                   self.o, self.o_scales, self.yp if self.probs_in_mlp else None, stream=stream)
         rec(3)
         self.call_combine(stream, slot)
         rec(4)
@@ -282,8 +286,10 @@ class Problem:
             self.moe.moe_combine_unpermute(self.handle, self.shape, self.layout, self.y, self.yp, io["out"],
                                            stream=stream)
         else:
+            # probabilities applied inside the MLP: the combine sums the rows unweighted
             self.moe.moe_combine_unpermute_fmt(self.handle, self.shape, self.layout, self.cfmt, self.o,
-                                               self.o_scales, self.yp, io["out"], stream=stream)
+                                               self.o_scales, None if self.probs_in_mlp else self.yp, io["out"],
+                                               stream=stream)
 
     def kernels_per_step(self) -> int:
         return 2 + 1 + (0 if self.identity else self.mlp_kernels) + 1
@@ -423,7 +429,7 @@ def run_ours(args, w):
         dist.barrier()
     import permute_grouped_expert_gb300 as moe
 
-    prob = Problem(moe, w, args.seed + rank, dev, args.combine_format)
+    prob = Problem(moe, w, args.seed + rank, dev, args.combine_format, args.probs_in_mlp)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
 
@@ -643,6 +649,7 @@ def run_ours(args, w):
         "config": {"workload": w.name, "tokens": w.T, "hidden": w.H, "experts": w.E, "topk": w.K,
                    "intermediate": w.I, "pad_multiple": w.m, "routing": w.routing,
                    "combine_format": args.combine_format,
+                   "probs_applied": "in the MLP (FC2 epilogue)" if args.probs_in_mlp else "in the combine",
                    "capacity_factor": w.cap_factor or None, "capacity": prob.cap,
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2)"
                    if in_bytes > L2_BYTES else "inputs smaller than L2 (no flush)",
@@ -656,7 +663,7 @@ def run_ours(args, w):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed, sample_tokens=args.cpu_sample_tokens,
-                                            target_s=args.cpu_seconds)
+                                            target_s=args.cpu_seconds, probs_in_mlp=args.probs_in_mlp)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -706,7 +713,7 @@ class OracleWeights:
         return stack(0), stack(1), stack(2), stack(3), g
 
 
-def cpu_baseline(w, seed, sample_tokens=16, target_s=None, weights=None):
+def cpu_baseline(w, seed, sample_tokens=16, target_s=None, weights=None, probs_in_mlp=False):
     """The oracle as it stands, on a bounded sample: full preprocess and dispatch
     (with the activation quantization of FP8 / NVFP4 workloads; they scale with
     T), then the MLP and combine for sampled tokens (all their routes),
@@ -715,7 +722,9 @@ def cpu_baseline(w, seed, sample_tokens=16, target_s=None, weights=None):
     are outside the timed parts.  Without target_s the sample is
     `sample_tokens` tokens; with it, batches of new tokens (starting at one and
     growing with the measured rate) are added until the sampled part has taken
-    target_s seconds or every token is in.  Returns the cpu_baseline object."""
+    target_s seconds or every token is in.  probs_in_mlp: the MLP scales its FC2
+    rows by the probabilities and the combine sums them unweighted.  Returns the
+    cpu_baseline object."""
     import oracle
 
     oracle.build()
@@ -784,10 +793,11 @@ def cpu_baseline(w, seed, sample_tokens=16, target_s=None, weights=None):
         if w.I:
             ob, _ = oracle.grouped_mlp_rows(fmt_mlp, yq[sel], None if ys is None else ys[sel], w.H, w.I,
                                             len(experts), np.array(off, np.int32), w13q, s13, w2q, s2,
-                                            np.arange(len(sel)), **extra)
+                                            np.arange(len(sel)), row_probs=local_probs if probs_in_mlp else None,
+                                            **extra)
         else:
             ob = yq[sel]
-        oracle.combine(ob, local_row_of, local_probs)
+        oracle.combine(ob, local_row_of, None if probs_in_mlp else local_probs)
         t_sample += time.perf_counter() - t1
         done += n
         if target_s is None or t_sample >= target_s:
@@ -810,11 +820,13 @@ def run_reference(args, w):
     K, W = args.steps, args.warmup
     weights = OracleWeights(w, args.seed)
     for _ in range(W):
-        cpu_baseline(w, args.seed, sample_tokens=args.ref_sample_tokens, weights=weights)
+        cpu_baseline(w, args.seed, sample_tokens=args.ref_sample_tokens, weights=weights,
+                     probs_in_mlp=args.probs_in_mlp)
     vals = []
     t0 = time.perf_counter()
     for _ in range(K):
-        vals.append(cpu_baseline(w, args.seed, sample_tokens=args.ref_sample_tokens, weights=weights))
+        vals.append(cpu_baseline(w, args.seed, sample_tokens=args.ref_sample_tokens, weights=weights,
+                                 probs_in_mlp=args.probs_in_mlp))
     wall = time.perf_counter() - t0
     v = statistics.mean(x["value"] for x in vals)
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s",
@@ -826,7 +838,8 @@ def run_reference(args, w):
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes of the pages' workloads)",
             "config": {"workload": w.name, "tokens": w.T, "hidden": w.H, "experts": w.E, "topk": w.K,
-                       "intermediate": w.I},
+                       "intermediate": w.I,
+                       "probs_applied": "in the MLP (FC2 epilogue)" if args.probs_in_mlp else "in the combine"},
             "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
                              "sample": vals[0]["sample"] + f"; {K} timed samples, {wall:.1f} s wall"},
             "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -842,6 +855,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--combine-format", default="bf16", choices=["bf16", "mxfp8", "mxfp4"],
                     help="format of the expert-output rows the combine reads (MX formats: FP8 path only)")
+    ap.add_argument("--probs-in-mlp", action="store_true",
+                    help="apply the routing probabilities in the MLP's FC2 epilogue; the combine sums unweighted")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16, help="batch-size scale of the CPU oracle sample")

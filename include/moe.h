@@ -391,22 +391,32 @@ MOE_API moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape
                            const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
                            size_t workspace_bytes, void* out_fc2, void* stream);
 
-/* moe_grouped_mlp with FC2 rows written in a combine format ([MEGAMOE], commit
- * list: "fp8 combine may use the bulk fc2 store"): out_format
- * MOE_COMBINE_BF16 behaves exactly as moe_grouped_mlp (out_fc2_scales
- * ignored); MOE_COMBINE_MXFP8 / MOE_COMBINE_MXFP4 make FC2's epilogue encode
- * each row's fp32 sums into codes at out_fc2 and E8M0 scales at out_fc2_scales
- * (device [cap][H/32] bytes, 4-byte aligned), layouts as documented with
- * MOE_COMBINE_*.  The MX formats are written by the FP8 path
- * (w_dtype MOE_DTYPE_FP8_E4M3_B128); other w_dtype values return
- * MOE_ERR_UNSUPPORTED with them (write bf16 and convert with
- * moe_quantize_mx_rows). */
-MOE_API moe_status moe_grouped_mlp_fmt(const moe_handle_dev* handle, const moe_shape* shape,
-                                       const moe_layout* layout, int32_t w_dtype, const void* perm_tokens,
-                                       const void* perm_scales, const void* w13, const void* w13_scales,
-                                       const void* w2, const void* w2_scales, const moe_nvfp4_globals* globals,
-                                       void* workspace, size_t workspace_bytes, int32_t out_format, void* out_fc2,
-                                       void* out_fc2_scales, void* stream);
+/* moe_grouped_mlp with two extensions.
+ * (1) FC2 rows written in a combine format ([MEGAMOE], commit list: "fp8
+ * combine may use the bulk fc2 store"): out_format MOE_COMBINE_BF16 writes bf16
+ * as moe_grouped_mlp does (out_fc2_scales ignored); MOE_COMBINE_MXFP8 /
+ * MOE_COMBINE_MXFP4 make FC2's epilogue encode each row's fp32 sums into codes
+ * at out_fc2 and E8M0 scales at out_fc2_scales (device [cap][H/32] bytes,
+ * 4-byte aligned), layouts as documented with MOE_COMBINE_*.  The MX formats
+ * are written by the FP8 path (w_dtype MOE_DTYPE_FP8_E4M3_B128); other w_dtype
+ * values return MOE_ERR_UNSUPPORTED with them (write bf16 and convert with
+ * moe_quantize_mx_rows).
+ * (2) Probabilities applied inside the MLP ([ALLGATHER], Testing: the
+ * dispatched probabilities reach the experts and their gradients flow back
+ * through the dispatch): fc2_row_probs, when not NULL, is device fp32 [cap]
+ * (4-byte aligned) indexed by permuted row -- the perm_probs that
+ * moe_dispatch_permute wrote -- and FC2's epilogue multiplies every row r by
+ * fc2_row_probs[r] in fp32 before the row is rounded to its output format:
+ *   out_fc2[r] = fmt( fc2_row_probs[r] * (act . w2[e]^T) ).
+ * The layer is then completed by a combine without weights
+ * (moe_combine_unpermute with perm_probs NULL).  Every w_dtype and out_format
+ * supports it.  NULL gives moe_grouped_mlp's rows. */
+MOE_API moe_status moe_grouped_mlp_ex(const moe_handle_dev* handle, const moe_shape* shape,
+                                      const moe_layout* layout, int32_t w_dtype, const void* perm_tokens,
+                                      const void* perm_scales, const void* w13, const void* w13_scales,
+                                      const void* w2, const void* w2_scales, const moe_nvfp4_globals* globals,
+                                      void* workspace, size_t workspace_bytes, int32_t out_format, void* out_fc2,
+                                      void* out_fc2_scales, const float* fc2_row_probs, void* stream);
 
 /* Number of kernels one moe_grouped_mlp call with these arguments launches
  * (host only, no device access): 1 where FC1 and FC2 run in one persistent

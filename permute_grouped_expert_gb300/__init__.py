@@ -101,9 +101,9 @@ _SIGNATURES = {
     "moe_grouped_mlp": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                         ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Nvfp4Globals), _P,
                         ctypes.c_size_t, _P, _P],
-    "moe_grouped_mlp_fmt": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
-                            ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Nvfp4Globals), _P,
-                            ctypes.c_size_t, ctypes.c_int32, _P, _P, _P],
+    "moe_grouped_mlp_ex": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
+                           ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Nvfp4Globals), _P,
+                           ctypes.c_size_t, ctypes.c_int32, _P, _P, _P, _P],
     "moe_combine_unpermute_fmt": [ctypes.POINTER(_HandleDev), ctypes.POINTER(_Shape), ctypes.POINTER(_Layout),
                                   ctypes.c_int32, _P, _P, _P, _P, _P],
     "moe_quantize_mx_rows": [_P, _I64, _I64, ctypes.c_int32, _P, _P, _P],
@@ -324,17 +324,19 @@ def moe_grouped_mlp(handle: Handle, shape: Shape, layout: Layout, w_dtype: int, 
            "moe_grouped_mlp")
 
 
-def moe_grouped_mlp_fmt(handle: Handle, shape: Shape, layout: Layout, w_dtype: int, perm_tokens: torch.Tensor,
-                        perm_scales: Optional[torch.Tensor], w13: torch.Tensor, w13_scales: Optional[torch.Tensor],
-                        w2: torch.Tensor, w2_scales: Optional[torch.Tensor], globals_: Optional[Nvfp4Globals],
-                        workspace: torch.Tensor, out_format: int, out_fc2: torch.Tensor,
-                        out_fc2_scales: Optional[torch.Tensor], stream=None) -> None:
+def moe_grouped_mlp_ex(handle: Handle, shape: Shape, layout: Layout, w_dtype: int, perm_tokens: torch.Tensor,
+                       perm_scales: Optional[torch.Tensor], w13: torch.Tensor, w13_scales: Optional[torch.Tensor],
+                       w2: torch.Tensor, w2_scales: Optional[torch.Tensor], globals_: Optional[Nvfp4Globals],
+                       workspace: torch.Tensor, out_format: int, out_fc2: torch.Tensor,
+                       out_fc2_scales: Optional[torch.Tensor] = None, fc2_row_probs: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
     g = ctypes.byref(globals_.c()) if globals_ is not None else None
-    _check(_lib.moe_grouped_mlp_fmt(ctypes.byref(handle.c()), ctypes.byref(shape.c()), ctypes.byref(layout.c()),
-                                    w_dtype, _ptr(perm_tokens), _ptr(perm_scales), _ptr(w13), _ptr(w13_scales),
-                                    _ptr(w2), _ptr(w2_scales), g, _ptr(workspace),
-                                    workspace.numel() * workspace.element_size(), out_format, _ptr(out_fc2),
-                                    _ptr(out_fc2_scales), _stream(stream)), "moe_grouped_mlp_fmt")
+    _check(_lib.moe_grouped_mlp_ex(ctypes.byref(handle.c()), ctypes.byref(shape.c()), ctypes.byref(layout.c()),
+                                   w_dtype, _ptr(perm_tokens), _ptr(perm_scales), _ptr(w13), _ptr(w13_scales),
+                                   _ptr(w2), _ptr(w2_scales), g, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), out_format, _ptr(out_fc2),
+                                   _ptr(out_fc2_scales), _ptr(fc2_row_probs), _stream(stream)),
+           "moe_grouped_mlp_ex")
 
 
 def moe_combine_unpermute_fmt(handle: Handle, shape: Shape, layout: Layout, in_format: int,

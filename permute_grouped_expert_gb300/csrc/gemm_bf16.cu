@@ -85,6 +85,7 @@ struct FusedParams {
   int32_t* status;         // device status word (timeouts)
   int32_t* sched;          // tile claim counter, zeroed before the launch
   int32_t* ready;          // [token tiles] FC1 completions per token tile, zeroed before the launch
+  const float* fc2_probs;  // [cap] probability multiplied into each FC2 row, or NULL
   PhaseParams ph[2];
   int E, cap;
   int ready_target;  // kEpiWarps * FC1 feature tiles: a token tile's intermediate rows are complete
@@ -438,6 +439,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
             tmem_ld32(taddr + h * BT + c * 32, v);
             const int rows_valid = (int)min64(ti.row_end - (ti.row0 + c * 32), 32);
+            if (p.fc2_probs) {
+              // lane j fetches token j's probability; every lane scales its feature of the 32 tokens
+              const float pr = lane < rows_valid ? p.fc2_probs[ti.row0 + c * 32 + lane] : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 32; j++) v[j] *= __shfl_sync(0xffffffffu, pr, j);
+            }
             transpose_store32(patch, v, dst0 + (int64_t)c * 32 * row_bytes, row_bytes, rows_valid, lane);
           }
         }
@@ -487,7 +494,8 @@ size_t grouped_mlp_bf16_ready_bytes(const moe_shape& s, const moe_layout& l) {
 // is running or done.
 cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                     const void* perm_tokens, const void* w13, const void* w2, void* act,
-                                    void* ready, void* out_fc2, cudaStream_t st, int64_t silent_token_tile) {
+                                    void* ready, void* out_fc2, const float* fc2_probs, cudaStream_t st,
+                                    int64_t silent_token_tile) {
   if (l.capacity == 0) return cudaSuccess;
   if (s.E > kMaxE) return cudaErrorNotSupported;
   const uint64_t cap = (uint64_t)l.capacity;
@@ -517,6 +525,7 @@ cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s,
   p.status = h.status;
   p.sched = static_cast<int32_t*>(ready);
   p.ready = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ready) + kSchedBytes);
+  p.fc2_probs = fc2_probs;
   p.E = (int)s.E;
   p.cap = (int)l.capacity;
   PhaseParams& p1 = p.ph[0];

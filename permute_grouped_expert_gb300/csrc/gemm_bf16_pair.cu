@@ -50,6 +50,7 @@ struct PairParams {
   const int32_t* offsets;     // [E+1] padded segment offsets
   int32_t* status;
   uint8_t* out;               // bf16 output [cap][ld_out]
+  const float* row_probs;     // [cap] probability multiplied into each output row (FC2), or NULL
   int64_t ld_out;
   int64_t out_cols;
   int64_t b_rows_per_expert;  // 2I (FC1) or H (FC2)
@@ -296,10 +297,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       } else {
         uint8_t* dst = p.out + (row * p.ld_out + (int64_t)ti.n * BN) * 2;
+        const float pr = p.row_probs && valid ? p.row_probs[row] : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < 8; c++) {
           float v[32];
           tmem_ld32(taddr + c * 32, v);
+          if (p.row_probs) {
+#pragma unroll
+            for (int j = 0; j < 32; j++) v[j] *= pr;
+          }
           if (valid && (int64_t)ti.n * BN + c * 32 < p.out_cols) store_row32(dst + c * 64, v);
         }
       }
@@ -346,7 +352,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Pair
 
 cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                          const void* perm_tokens, const void* w13, const void* w2, void* act,
-                                         void* out_fc2, cudaStream_t st) {
+                                         void* out_fc2, const float* fc2_probs, cudaStream_t st) {
   if (l.capacity == 0) return cudaSuccess;
   if (s.E > kMaxE) return cudaErrorNotSupported;
   const uint64_t cap = (uint64_t)l.capacity;
@@ -371,6 +377,7 @@ cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shap
   p1.offsets = h.padded_offsets;
   p1.status = h.status;
   p1.out = static_cast<uint8_t*>(act);
+  p1.row_probs = nullptr;
   p1.ld_out = s.I;
   p1.out_cols = s.I;
   p1.b_rows_per_expert = 2 * s.I;
@@ -385,6 +392,7 @@ cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shap
 
   PairParams p2 = p1;
   p2.out = static_cast<uint8_t*>(out_fc2);
+  p2.row_probs = fc2_probs;
   p2.ld_out = s.H;
   p2.out_cols = s.H;
   p2.b_rows_per_expert = s.H;

@@ -116,6 +116,7 @@ struct Fp8Params {
   int E, cap, nt, nkb, n_blocks_b;  // n_blocks_b = weight rows / 128 per expert
   int out_format;            // FC2: MOE_COMBINE_BF16 / _MXFP8 / _MXFP4
   uint8_t* out_mx_scales;    // FC2 in an MX format: E8M0 [cap][H/32]
+  const float* row_probs;    // FC2: [cap] probability multiplied into each output row, or NULL
 };
 
 // Shared exponent X of an MX block with magnitude maximum amax: floor(log2(amax))
@@ -452,6 +453,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const bool valid = row < ti.row_end && !ti.masked;
       float* acc = reinterpret_cast<float*>(acc2);
+      if (kMode == kFc2 && p.row_probs) {
+        // the route's probability scales the row before it is rounded to the output format
+        const float pr = valid ? __ldg(p.row_probs + row) : 0.0f;
+        const float2 pr2 = make_float2(pr, pr);
+#pragma unroll
+        for (int j = 0; j < 64; j++) acc2[j] = __fmul2_rn(acc2[j], pr2);
+      }
       if (kMode == kFc1SwiGLU) {
         // acc[0..63] = up, acc[64..127] = gate of output columns n*128 + 64*grp + j
         float amax = 0.0f;
@@ -578,7 +586,8 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                    const void* perm_codes, const void* perm_scales, const void* w13,
                                    const void* w13_scales, const void* w2, const void* w2_scales, void* workspace,
-                                   void* out_fc2, int32_t out_format, void* out_fc2_scales, cudaStream_t st) {
+                                   void* out_fc2, int32_t out_format, void* out_fc2_scales,
+                                   const float* fc2_probs, cudaStream_t st) {
   if (l.capacity == 0) return cudaSuccess;
   if (s.E > kMaxE) return cudaErrorNotSupported;
   const uint64_t cap = (uint64_t)l.capacity;
@@ -622,6 +631,7 @@ cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, 
   p1.n_blocks_b = (int)(2 * s.I / 128);
   p1.out_format = MOE_COMBINE_BF16;
   p1.out_mx_scales = nullptr;
+  p1.row_probs = nullptr;
   if ((e = launch_one<kFc1SwiGLU>(ta1, ta1h, tb1, p1, m_tiles_bound * p1.nt, st)) != cudaSuccess) return e;
   if (prof.after_fc1 && (e = record_profile_event(prof.after_fc1, st)) != cudaSuccess) return e;
 
@@ -639,6 +649,7 @@ cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, 
   p2.n_blocks_b = (int)(s.H / 128);
   p2.out_format = out_format;
   p2.out_mx_scales = static_cast<uint8_t*>(out_fc2_scales);
+  p2.row_probs = fc2_probs;
   if ((e = launch_one<kFc2>(ta2, ta2h, tb2, p2, m_tiles_bound * p2.nt, st)) != cudaSuccess) return e;
   if (prof.after_fc2 && (e = record_profile_event(prof.after_fc2, st)) != cudaSuccess) return e;
   return cudaSuccess;

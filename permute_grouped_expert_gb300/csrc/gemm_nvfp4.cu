@@ -42,6 +42,7 @@ using namespace sm100;
 
 constexpr int BMW = 128;        // weight rows per tile (MMA M)
 constexpr int BNT = 32;         // tokens per tile (MMA N)
+static_assert(BNT == 32, "the FC2 epilogue hands one token per lane");
 constexpr int BKR = 256;        // K elements per raw stage
 constexpr int BKC = 64;         // K elements per converted slice (one 128-byte swizzle atom of f16)
 constexpr int kRawStages = 4;
@@ -119,6 +120,7 @@ struct Fp4Params {
   const float* x_global;   // [1] global scale of the token operand
   const float* w_global;   // [E] global scale of the weights
   const float* out_global; // FC1: [1] global scale the intermediate is encoded with
+  const float* row_probs;  // FC2: [cap] probability multiplied into each token row, or NULL
   int64_t ld_out;          // elements per output row
   int64_t w_rows_per_expert;
   int64_t gate_offset;     // FC1: I
@@ -524,6 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kMode == kFc2) {
         const int64_t col = (int64_t)ti.mt * BMW + wr;
         uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
+        if (p.row_probs) {
+          // lane j fetches token j's probability; every lane scales its feature of the 32 tokens
+          const float pr = ti.row0 + lane < ti.row_end ? __ldg(p.row_probs + ti.row0 + lane) : 0.0f;
+#pragma unroll
+          for (int j = 0; j < BNT; j++) v[j] *= __shfl_sync(0xffffffffu, pr, j);
+        }
 #pragma unroll
         for (int j = 0; j < BNT; j++) {
           const int64_t row = ti.row0 + j;
@@ -601,7 +609,8 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                      const void* perm_packed, const void* perm_scales, const void* w13,
                                      const void* w13_scales, const void* w2, const void* w2_scales,
-                                     const moe_nvfp4_globals& g, void* workspace, void* out_fc2, cudaStream_t st) {
+                                     const moe_nvfp4_globals& g, void* workspace, void* out_fc2,
+                                     const float* fc2_probs, cudaStream_t st) {
   if (l.capacity == 0) return cudaSuccess;
   if (s.E > kMaxE || s.H % BKR != 0 || s.I % BKR != 0) return cudaErrorNotSupported;
   const uint64_t cap = (uint64_t)l.capacity;
@@ -633,6 +642,7 @@ cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s
   p1.x_global = g.fc1_input_scale;
   p1.w_global = g.w13_scale_2;
   p1.out_global = g.fc2_input_scale;
+  p1.row_probs = nullptr;
   p1.ld_out = s.I;
   p1.w_rows_per_expert = 2 * s.I;
   p1.gate_offset = s.I;
@@ -649,6 +659,7 @@ cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s
   p2.x_global = g.fc2_input_scale;
   p2.w_global = g.w2_scale_2;
   p2.out_global = nullptr;
+  p2.row_probs = fc2_probs;
   p2.ld_out = s.H;
   p2.w_rows_per_expert = s.H;
   p2.gate_offset = 0;

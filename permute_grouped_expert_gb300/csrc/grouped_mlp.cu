@@ -6,22 +6,25 @@ namespace moe {
 
 cudaError_t launch_grouped_mlp_bf16(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                     const void* perm_tokens, const void* w13, const void* w2, void* act,
-                                    void* ready, void* out_fc2, cudaStream_t st, int64_t silent_token_tile);
+                                    void* ready, void* out_fc2, const float* fc2_probs, cudaStream_t st,
+                                    int64_t silent_token_tile);
 size_t grouped_mlp_bf16_ready_bytes(const moe_shape& s, const moe_layout& l);
 
 cudaError_t launch_grouped_mlp_bf16_pair(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                          const void* perm_tokens, const void* w13, const void* w2, void* act,
-                                         void* out_fc2, cudaStream_t st);
+                                         void* out_fc2, const float* fc2_probs, cudaStream_t st);
 
 cudaError_t launch_grouped_mlp_fp8(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                    const void* perm_codes, const void* perm_scales, const void* w13,
                                    const void* w13_scales, const void* w2, const void* w2_scales, void* workspace,
-                                   void* out_fc2, int32_t out_format, void* out_fc2_scales, cudaStream_t st);
+                                   void* out_fc2, int32_t out_format, void* out_fc2_scales, const float* fc2_probs,
+                                   cudaStream_t st);
 
 cudaError_t launch_grouped_mlp_nvfp4(const moe_handle_dev& h, const moe_shape& s, const moe_layout& l,
                                      const void* perm_packed, const void* perm_scales, const void* w13,
                                      const void* w13_scales, const void* w2, const void* w2_scales,
-                                     const moe_nvfp4_globals& g, void* workspace, void* out_fc2, cudaStream_t st);
+                                     const moe_nvfp4_globals& g, void* workspace, void* out_fc2,
+                                     const float* fc2_probs, cudaStream_t st);
 
 namespace {
 constexpr int64_t kPairMinRowsPerExpert = 4096;
@@ -66,23 +69,23 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                const void* w13, const void* w13_scales, const void* w2,
                                const void* w2_scales, const moe_nvfp4_globals* globals,
                                void* workspace, void* out_fc2, int32_t out_format, void* out_fc2_scales,
-                               cudaStream_t st) {
+                               const float* fc2_probs, cudaStream_t st) {
   const int64_t silent = take_debug_mlp_silent_tile();  // testing hook: only the fused bf16 kernel uses it
   // MX combine formats are written by the FP8 path's FC2 epilogue only
   if (out_format != MOE_COMBINE_BF16 && w_dtype != MOE_DTYPE_FP8_E4M3_B128) return cudaErrorNotSupported;
   switch (w_dtype) {
     case MOE_DTYPE_BF16:
       if (grouped_mlp_bf16_uses_pairs(s, l))
-        return launch_grouped_mlp_bf16_pair(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, st);
+        return launch_grouped_mlp_bf16_pair(h, s, l, perm_tokens, w13, w2, workspace, out_fc2, fc2_probs, st);
       return launch_grouped_mlp_bf16(h, s, l, perm_tokens, w13, w2, workspace,
                                      static_cast<uint8_t*>(workspace) + round_up((size_t)l.capacity * s.I * 2, 1024),
-                                     out_fc2, st, silent);
+                                     out_fc2, fc2_probs, st, silent);
     case MOE_DTYPE_FP8_E4M3_B128:
       return launch_grouped_mlp_fp8(h, s, l, perm_tokens, perm_scales, w13, w13_scales, w2, w2_scales, workspace,
-                                    out_fc2, out_format, out_fc2_scales, st);
+                                    out_fc2, out_format, out_fc2_scales, fc2_probs, st);
     case MOE_DTYPE_NVFP4:
       return launch_grouped_mlp_nvfp4(h, s, l, perm_tokens, perm_scales, w13, w13_scales, w2, w2_scales, *globals,
-                                      workspace, out_fc2, st);
+                                      workspace, out_fc2, fc2_probs, st);
     default:
       return cudaErrorNotSupported;
   }

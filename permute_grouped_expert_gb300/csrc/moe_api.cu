@@ -345,21 +345,22 @@ moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape,
                            const void* w13, const void* w13_scales, const void* w2,
                            const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
                            size_t workspace_bytes, void* out_fc2, void* stream) {
-  return moe_grouped_mlp_fmt(handle, shape, layout, w_dtype, perm_tokens, perm_scales, w13, w13_scales, w2,
-                             w2_scales, globals, workspace, workspace_bytes, MOE_COMBINE_BF16, out_fc2, nullptr,
-                             stream);
+  return moe_grouped_mlp_ex(handle, shape, layout, w_dtype, perm_tokens, perm_scales, w13, w13_scales, w2,
+                            w2_scales, globals, workspace, workspace_bytes, MOE_COMBINE_BF16, out_fc2, nullptr,
+                            nullptr, stream);
 }
 
-moe_status moe_grouped_mlp_fmt(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
-                               int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
-                               const void* w13, const void* w13_scales, const void* w2,
-                               const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
-                               size_t workspace_bytes, int32_t out_format, void* out_fc2, void* out_fc2_scales,
-                               void* stream) {
+moe_status moe_grouped_mlp_ex(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,
+                              int32_t w_dtype, const void* perm_tokens, const void* perm_scales,
+                              const void* w13, const void* w13_scales, const void* w2,
+                              const void* w2_scales, const moe_nvfp4_globals* globals, void* workspace,
+                              size_t workspace_bytes, int32_t out_format, void* out_fc2, void* out_fc2_scales,
+                              const float* fc2_row_probs, void* stream) {
   if (out_format != MOE_COMBINE_BF16 && out_format != MOE_COMBINE_MXFP8 && out_format != MOE_COMBINE_MXFP4)
     return MOE_ERR_INVALID_ARG;
   if (out_format != MOE_COMBINE_BF16 && (!out_fc2_scales || (reinterpret_cast<uintptr_t>(out_fc2_scales) & 3u)))
     return MOE_ERR_INVALID_ARG;
+  if (fc2_row_probs && (reinterpret_cast<uintptr_t>(fc2_row_probs) & 3u)) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_handle(handle));
   MOE_TRY(check_shape(shape, true));
   MOE_TRY(check_layout(layout));
@@ -386,7 +387,7 @@ moe_status moe_grouped_mlp_fmt(const moe_handle_dev* handle, const moe_shape* sh
   if (workspace_bytes < grouped_mlp_workspace_bytes(*shape, *layout, w_dtype)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaError_t e = launch_grouped_mlp(*handle, *shape, *layout, w_dtype, perm_tokens, perm_scales, w13,
                                      w13_scales, w2, w2_scales, globals, workspace, out_fc2, out_format,
-                                     out_fc2_scales, static_cast<cudaStream_t>(stream));
+                                     out_fc2_scales, fc2_row_probs, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }

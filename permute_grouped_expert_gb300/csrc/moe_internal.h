@@ -76,7 +76,7 @@ cudaError_t launch_grouped_mlp(const moe_handle_dev& h, const moe_shape& s, cons
                                const void* w13, const void* w13_scales, const void* w2,
                                const void* w2_scales, const moe_nvfp4_globals* globals,
                                void* workspace, void* out_fc2, int32_t out_format, void* out_fc2_scales,
-                               cudaStream_t st);
+                               const float* fc2_row_probs, cudaStream_t st);
 cudaError_t launch_combine_mx(const moe_handle_dev& h, const moe_shape& s, int32_t in_format,
                               const void* codes, const void* scales, const float* perm_probs, void* y,
                               cudaStream_t st);

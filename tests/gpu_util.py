@@ -133,12 +133,13 @@ def largest_expert_rows(pre, cap, n):
     return np.unique(np.linspace(beg, end - 1, n).astype(np.int64)), e
 
 
-def oracle_rows_chunked(oracle, fmt, yq, ys, pre, rows, H, I, expert_weights, chunk=16, **globs):
+def oracle_rows_chunked(oracle, fmt, yq, ys, pre, rows, H, I, expert_weights, chunk=16, perm_probs=None, **globs):
     """Oracle FFN of the given permuted rows, a chunk of experts at a time so
     that only that chunk's oracle-format weights are in host memory.
     expert_weights(experts) -> (w13, w13_scales, w2, w2_scales, g13, g2) for
     those experts in the oracle's format (g13 / g2 None except NVFP4).
-    Returns (rows in evaluation order, bf16 outputs [n, H])."""
+    perm_probs ([cap], optional): probabilities applied to the FC2 rows inside
+    the MLP.  Returns (rows in evaluation order, bf16 outputs [n, H])."""
     rows = np.unique(np.asarray(rows, np.int64))
     owner = expert_of_rows(pre["offsets"], rows)
     experts = sorted(set(owner.tolist()))
@@ -155,6 +156,8 @@ def oracle_rows_chunked(oracle, fmt, yq, ys, pre, rows, H, I, expert_weights, ch
         extra = dict(globs)
         if g13 is not None:
             extra.update(w13_global=g13, w2_global=g2)
+        if perm_probs is not None:
+            extra["row_probs"] = np.asarray(perm_probs, np.float32)[sel]
         ob, _ = oracle.grouped_mlp_rows(fmt, yq[sel], None if ys is None else ys[sel], H, I, len(ex),
                                         np.array(off, np.int32), q13, s13, q2, s2, np.arange(len(sel)), **extra)
         sel_all.append(sel)

@@ -162,6 +162,16 @@ def test_validation_rejects_before_any_launch(moe):
     assert lib.moe_grouped_mlp(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16, fake, None,
                                fake, None, fake, None, None, fake, 8, fake,
                                None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    # extended grouped MLP: misaligned FC2 row probabilities, unknown output format, MX output without scales
+    assert lib.moe_grouped_mlp_ex(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16, fake, None,
+                                  fake, None, fake, None, None, fake, 1 << 30, moe.COMBINE_BF16, fake, None,
+                                  ctypes.c_void_p(0x1002), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_mlp_ex(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16, fake, None,
+                                  fake, None, fake, None, None, fake, 1 << 30, 9, fake, None, fake,
+                                  None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_mlp_ex(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_FP8_E4M3_B128,
+                                  fake, fake, fake, fake, fake, fake, None, fake, 1 << 30, moe.COMBINE_MXFP8, fake,
+                                  None, fake, None) == moe.MOE_ERR_INVALID_ARG
     # backward calls: null gradient buffers, probability gradients without their inputs, unknown routing format
     assert lib.moe_combine_backward(byref(handle), byref(good_shape), byref(good_layout), fake, fake, fake, None,
                                     None, None) == moe.MOE_ERR_INVALID_ARG

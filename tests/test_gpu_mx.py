@@ -96,7 +96,7 @@ def _run_fp8_layer_mx(moe, w, seed, elem):
     oc = fill_pattern(torch.empty(cap, w.H if elem == 0 else w.H // 2, dtype=torch.uint8, device="cuda"))
     osc = fill_pattern(torch.empty(cap, w.H // 32, dtype=torch.uint8, device="cuda"))
     ofmt = moe.COMBINE_MXFP8 if elem == 0 else moe.COMBINE_MXFP4
-    moe.moe_grouped_mlp_fmt(handle, shape, layout, moe.DTYPE_FP8_E4M3_B128, y, ys, q13, s13, q2, s2, None, ws, ofmt,
+    moe.moe_grouped_mlp_ex(handle, shape, layout, moe.DTYPE_FP8_E4M3_B128, y, ys, q13, s13, q2, s2, None, ws, ofmt,
                             oc, osc)
     out = fill_pattern(torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda"))
     moe.moe_combine_unpermute_fmt(handle, shape, layout, ofmt, oc, osc, yp, out)
@@ -168,6 +168,6 @@ def test_mx_output_unsupported_on_bf16_path(moe):
     h = moe.Handle.empty(shape, layout)
     buf = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     with pytest.raises(moe.MoeError) as ei:
-        moe.moe_grouped_mlp_fmt(h, shape, layout, moe.DTYPE_BF16, buf, None, buf, None, buf, None, None, buf,
+        moe.moe_grouped_mlp_ex(h, shape, layout, moe.DTYPE_BF16, buf, None, buf, None, buf, None, None, buf,
                                 moe.COMBINE_MXFP8, buf, buf)
     assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
