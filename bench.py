@@ -671,6 +671,300 @@ def run_ours(args, w):
         print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------- backward
+
+class BackwardProblem:
+    """Buffers of the layer's backward through combine and dispatch: the combine
+    backward (gradient row per route, probability gradient per row) then the
+    dispatch backward (token gradients, probability gradients in the routing
+    layout).  The expert MLP's own backward is not part of this path, so the
+    dispatch backward takes the combine backward's row gradients as the
+    gradients of the dispatched rows (the whole layer's backward for identity
+    experts).  The forward state it needs -- the handle, the dispatched
+    probabilities and the expert rows -- comes from one forward step of `prob`."""
+
+    def __init__(self, prob, seed):
+        import torch
+
+        moe, w, dev = prob.moe, prob.w, prob.dev
+        if not prob.identity and prob.cfmt != moe.COMBINE_BF16:
+            raise SystemExit("--direction backward reads bf16 expert rows (--combine-format bf16)")
+        if prob.identity and w.dtype != "bf16":
+            raise SystemExit("--direction backward with identity experts needs bf16 rows")
+        self.prob, self.moe, self.w = prob, moe, w
+        self.o = prob.y if prob.identity else prob.o
+        self.gy_host = workloads.grad_outputs(w, seed).pin_memory()
+        self.gy = self.gy_host.to(dev)
+        cap = prob.cap
+        self.g_o = torch.empty(cap, w.H, dtype=torch.bfloat16, device=dev)
+        self.g_w = torch.empty(cap, dtype=torch.float32, device=dev)
+        self.g_x = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+        gp_shape = (w.T, w.K) if prob.fmt == moe.ROUTING_DENSE_I16 else (w.T, w.E)
+        self.g_p = torch.empty(gp_shape, dtype=torch.float32, device=dev)
+        self.slots = [dict(gy=self.gy, g_x=self.g_x, g_p=self.g_p,
+                           g_x_host=torch.empty(self.g_x.shape, dtype=torch.bfloat16).pin_memory(),
+                           g_p_host=torch.empty(gp_shape, dtype=torch.float32).pin_memory()),
+                      dict(gy=torch.empty_like(self.gy), g_x=torch.empty_like(self.g_x), g_p=torch.empty_like(self.g_p),
+                           g_x_host=torch.empty(self.g_x.shape, dtype=torch.bfloat16).pin_memory(),
+                           g_p_host=torch.empty(gp_shape, dtype=torch.float32).pin_memory())]
+
+    def call_combine_backward(self, stream, slot=0):
+        p = self.prob
+        self.moe.moe_combine_backward(p.handle, p.shape, p.layout, self.slots[slot]["gy"], self.o, p.yp, self.g_o,
+                                      self.g_w, stream=stream)
+
+    def call_dispatch_backward(self, stream, slot=0):
+        p, io = self.prob, self.slots[slot]
+        self.moe.moe_dispatch_backward(p.handle, p.shape, p.layout, p.fmt, self.g_o, self.g_w, io["g_x"],
+                                       io["g_p"], stream=stream)
+
+    def step(self, stream, ev=None, slot=0):
+        if ev:
+            ev[0].record(stream)
+        self.call_combine_backward(stream, slot)
+        if ev:
+            ev[1].record(stream)
+        self.call_dispatch_backward(stream, slot)
+        if ev:
+            ev[2].record(stream)
+
+    kernels_per_step = 3  # combine backward; dispatch backward = weight-1 combine + probability-gradient gather
+
+    def valid_rows(self):
+        import torch
+        torch.cuda.synchronize()
+        return min(int(self.prob.handle.total_rows.item()), self.prob.cap)
+
+    def combine_backward_bytes(self, R, V):
+        """gy read once, the routed expert rows read, gradient rows written for
+        routed and pad rows, one probability gradient per row, the row map and
+        the dispatched probabilities read."""
+        w = self.w
+        return w.T * w.H * 2 + R * w.H * 2 + V * w.H * 2 + V * 4 + R * 4 + w.T * w.K * 4
+
+    def dispatch_backward_bytes(self, R):
+        """Gradient rows read, token gradients written, the row map read twice,
+        row probability gradients read and written into the routing layout."""
+        w = self.w
+        return R * w.H * 2 + w.T * w.H * 2 + 2 * w.T * w.K * 4 + R * 4 + self.g_p.numel() * 4
+
+
+def run_backward(args, w):
+    import torch
+
+    import __graft_entry__
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    if rank == 0 or world == 1:
+        __graft_entry__.build_library()
+    if world > 1:
+        dist.barrier()
+    import permute_grouped_expert_gb300 as moe
+
+    prob = Problem(moe, w, args.seed + rank, dev, args.combine_format, args.probs_in_mlp)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        prob.step(stream)  # the forward state the backward reads
+    torch.cuda.synchronize()
+    bp = BackwardProblem(prob, args.seed + rank)
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            bp.step(stream)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: two graphs per step (combine backward, dispatch
+    # backward) with events between them, inputs resident in HBM
+    graphs = []
+    for fn in (bp.call_combine_backward, bp.call_dispatch_backward):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn(stream)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            graphs[0].replay()
+            graphs[1].replay()
+        for i in range(K):
+            evs[i][0].record(stream)
+            graphs[0].replay()
+            evs[i][1].record(stream)
+            graphs[1].replay()
+            evs[i][2].record(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(evs[0][0].elapsed_time(end), dev)
+    ms_step = total_ms / K
+    t_cb = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
+    t_db = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
+
+    # ---- end to end: each step copies dL/dy in from pinned host memory and the
+    # token and probability gradients back out (two slots, two copy streams)
+    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    compute_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    e0, e1, last_out = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                        torch.cuda.Event())
+    h2d = bp.gy_host.numel() * 2
+    d2h = bp.g_x.numel() * 2 + bp.g_p.numel() * 4
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    cin.wait_event(e0)
+    for i in range(K):
+        sl = i % 2
+        io = bp.slots[sl]
+        if i >= 2:
+            cin.wait_event(compute_done[sl])
+        with torch.cuda.stream(cin):
+            io["gy"].copy_(bp.gy_host, non_blocking=True)
+            in_done[sl].record(cin)
+        stream.wait_event(in_done[sl])
+        if i >= 2:
+            stream.wait_event(out_done[sl])
+        with torch.cuda.stream(stream):
+            bp.step(stream, slot=sl)
+            compute_done[sl].record(stream)
+        cout.wait_event(compute_done[sl])
+        with torch.cuda.stream(cout):
+            io["g_x_host"].copy_(io["g_x"], non_blocking=True)
+            io["g_p_host"].copy_(io["g_p"], non_blocking=True)
+            out_done[sl].record(cout)
+    last_out.record(cout)
+    stream.wait_event(last_out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+
+    R = prob.routed_rows()
+    V = bp.valid_rows()
+    peaks, peak_src = load_peaks()
+    cb_gbs = bp.combine_backward_bytes(R, V) / (statistics.mean(t_cb) * 1e-3) / 1e9
+    db_gbs = bp.dispatch_backward_bytes(R) / (statistics.mean(t_db) * 1e-3) / 1e9
+
+    def stats(xs):
+        return {"mean": round(statistics.mean(xs), 5), "min": round(min(xs), 5),
+                "median": round(statistics.median(xs), 5)}
+
+    cb_dominant = statistics.mean(t_cb) >= statistics.mean(t_db)
+    achieved = cb_gbs if cb_dominant else db_gbs
+    roof = {"kernel": "combine_backward" if cb_dominant else "dispatch_backward (weight-1 combine + gather)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": profiled_traffic(w.name + ":backward", "permute_grouped_expert_gb300/csrc/backward.cu"),
+            "peak_source": f"{peak_src} hbm_gbs",
+            "launch_ms": round(statistics.mean(t_cb if cb_dominant else t_db), 5)}
+    in_bytes = bp.combine_backward_bytes(R, V) + bp.dispatch_backward_bytes(R)
+    line = {
+        "metric": METRIC, "value": round(job_throughput(w.T, world, K, total_ms), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the pages' workloads)",
+        "config": {"workload": w.name, "direction": "backward (combine backward + dispatch backward)",
+                   "tokens": w.T, "hidden": w.H, "experts": w.E, "topk": w.K, "intermediate": w.I,
+                   "pad_multiple": w.m, "routing": w.routing, "capacity": prob.cap,
+                   "expert_backward": "not part of the path: the dispatch backward takes the combine backward's "
+                                      "row gradients" if not prob.identity else "identity experts",
+                   "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2)"
+                   if in_bytes > L2_BYTES else "inputs smaller than L2 (no flush)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "breakdown": {"combine_backward_ms": stats(t_cb), "dispatch_backward_ms": stats(t_db),
+                      "combine_backward_gbs": round(cb_gbs, 1), "dispatch_backward_gbs": round(db_gbs, 1),
+                      "combine_backward_frac_of_hbm": round(cb_gbs / peaks["hbm_gbs"], 4),
+                      "dispatch_backward_frac_of_hbm": round(db_gbs / peaks["hbm_gbs"], 4),
+                      "routed_rows": R, "valid_rows": V,
+                      "timing": "each step two CUDA graph replays (combine backward, dispatch backward) with "
+                                "events between them"},
+        "e2e": {"value": round(job_throughput(w.T, world, K, e2e_ms), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": bp.kernels_per_step * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_backward(BackwardOracleInputs(w, args.seed), target_s=args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+class BackwardOracleInputs:
+    """The oracle-side inputs of the backward, prepared once (not timed): the
+    routing, its preprocess, the expert rows (the oracle's dispatch of the
+    activations, standing in for the expert outputs: the cost does not depend
+    on the values) and dL/dy."""
+
+    def __init__(self, w, seed):
+        import oracle
+
+        oracle.build()
+        self.w = w
+        self.fmt, self.rmap, probs = workloads.routing_inputs(w, seed)
+        cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
+        if w.cap_factor:
+            cap = oracle.capacity(oracle.preprocess(self.fmt, self.rmap, w.T, w.E, w.K, w.m, cap)["total_rows"],
+                                  w.cap_factor)
+        self.pre = oracle.preprocess(self.fmt, self.rmap, w.T, w.E, w.K, w.m, cap)
+        self.o, self.po = oracle.dispatch(self.fmt, self.rmap, probs, self.pre,
+                                          workloads.bf16_bits(workloads.activations(w, seed)), cap, w.E, w.K)
+        self.gy = workloads.bf16_bits(workloads.grad_outputs(w, seed))
+
+
+def cpu_baseline_backward(inp, target_s=None, sample_tokens=64):
+    """The oracle's combine and dispatch backward as they stand, on a bounded
+    sample: batches of tokens (all their routes) until target_s seconds (or
+    sample_tokens tokens without a target), extrapolated to the batch.  Each
+    batch's rows are renumbered onto a compact list (the oracle's outputs are
+    sized by the rows it is given)."""
+    import oracle
+
+    w = inp.w
+    order = np.random.default_rng(0).permutation(w.T)
+    done, t = 0, 0.0
+    n = 1 if target_s is not None else sample_tokens
+    while done < w.T:
+        n = min(n, w.T - done)
+        toks = np.sort(order[done:done + n])
+        row_of = inp.pre["row_of"][toks]
+        sel = np.unique(row_of[row_of >= 0])
+        local = np.where(row_of >= 0, np.searchsorted(sel, np.where(row_of >= 0, row_of, 0)), -1).astype(np.int32)
+        sub = {"row_of": local, "counts": np.array([len(sel)], np.int32),
+               "offsets": np.array([0, len(sel)], np.int32)}
+        o_sel, po_sel, gy_sel, map_sel = inp.o[sel], inp.po[sel], inp.gy[toks], np.ascontiguousarray(inp.rmap[toks])
+        t0 = time.perf_counter()
+        g_o, g_w = oracle.combine_backward(gy_sel, sub, len(sel), o_sel, po_sel)
+        oracle.dispatch_backward(inp.fmt, map_sel, local, w.E, g_o, g_w)
+        t += time.perf_counter() - t0
+        done += n
+        if target_s is None or t >= target_s:
+            break
+        per_token = t / done
+        n = max(1, min(2 * done, int((target_s - t) / max(per_token, 1e-9)) + 1))
+    return {"value": round(done / t, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"combine backward + dispatch backward of {done} sampled tokens ({t:.2f} s) extrapolated "
+                      f"x{w.T / done:.1f}; routing preprocess, the row renumbering and input generation not timed"}
+
+
 # ----------------------------------------------------------- CPU oracle arm
 
 def _nvfp4_global(a) -> float:
@@ -818,6 +1112,9 @@ def run_reference(args, w):
     if rank != 0:
         return
     K, W = args.steps, args.warmup
+    if args.direction == "backward":
+        run_reference_backward(args, w)
+        return
     weights = OracleWeights(w, args.seed)
     for _ in range(W):
         cpu_baseline(w, args.seed, sample_tokens=args.ref_sample_tokens, weights=weights,
@@ -846,12 +1143,42 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_backward(args, w):
+    """The reference arm of the backward: the oracle's combine and dispatch
+    backward, each step a bounded sample of the batch's tokens."""
+    K, W = args.steps, args.warmup
+    inp = BackwardOracleInputs(w, args.seed)
+    for _ in range(W):
+        cpu_baseline_backward(inp, sample_tokens=args.ref_sample_tokens)
+    t0 = time.perf_counter()
+    vals = [cpu_baseline_backward(inp, sample_tokens=args.ref_sample_tokens) for _ in range(K)]
+    wall = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": K, "warmup": W,
+            "ms_per_step": round(w.T / v * 1e3, 3),
+            "timing": "each step runs the oracle's combine and dispatch backward on a bounded sample of the "
+                      "batch's tokens; value and ms_per_step are extrapolated to the whole batch",
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes of the pages' workloads)",
+            "config": {"workload": w.name, "direction": "backward (combine backward + dispatch backward)",
+                       "tokens": w.T, "hidden": w.H, "experts": w.E, "topk": w.K, "intermediate": w.I},
+            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"] + f"; {K} timed samples, {wall:.1f} s wall"},
+            "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="dsv3", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(workloads.WORKLOADS),
+                    help="default: dsv3 forward, permute backward")
+    ap.add_argument("--direction", default="forward", choices=["forward", "backward"],
+                    help="backward: the combine backward and the dispatch backward (the expert MLP's own "
+                         "backward is not part of the path)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--combine-format", default="bf16", choices=["bf16", "mxfp8", "mxfp4"],
                     help="format of the expert-output rows the combine reads (MX formats: FP8 path only)")
@@ -869,12 +1196,16 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload is None:
+        args.workload = "permute" if args.direction == "backward" else "dsv3"
     w = workloads.WORKLOADS[args.workload]
     if args.set:
         changes = {k: int(v) for k, v in (kv.split("=", 1) for kv in args.set)}
         w = workloads.scaled(w, name=w.name + "+" + ",".join(args.set), **changes)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.direction == "backward":
+        run_backward(args, w)
     else:
         run_ours(args, w)
 

@@ -144,6 +144,12 @@ def activations(w: Workload, seed: int, device: str = "cpu") -> torch.Tensor:
     return (x * w.x_std).to(torch.bfloat16)
 
 
+def grad_outputs(w: Workload, seed: int, device: str = "cpu") -> torch.Tensor:
+    """Gradient of the layer output, dL/dy ~ N(0, 1) rounded to bf16, [T, H]."""
+    g = torch.Generator(device=device).manual_seed(seed * 1000 + 4)
+    return torch.randn(w.T, w.H, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
 def expert_weights(w: Workload, seed: int, device: str = "cpu", experts=None):
     """bf16 (w13 [E, 2I, H], w2 [E, H, I]) ~ N(0, w_std), generated expert by expert.
 
