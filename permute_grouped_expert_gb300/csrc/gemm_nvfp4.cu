@@ -17,18 +17,18 @@
 // global scales (alpha = activation global x expert weight global) are applied
 // in the epilogue.
 //
-// One CTA per SM, 14 warps:
+// One CTA per SM, 16 warps:
 //   warp 0      TMA producer: raw stages of 256 K elements (packed weights
 //               128 rows x 128 B, their scales 128 x 16 B, packed tokens 32 x 128 B,
 //               their scales 32 x 16 B), 4 stages
 //   warp 1      TMEM allocation (2 x 32 fp32 columns) and MMA issue
-//   warps 2..9  converters: E2M1 + E4M3 -> f16, written in the 128-byte swizzled
-//               K-major layout the MMA reads, 64 K elements per converted stage
-//               (5 stages);
-//               each thread expands half a weight row (plus, for 64 threads, half
-//               a token row; token rows past the expert's end are skipped)
+//   warps 2..9  weight converters: E2M1 + E4M3 -> f16, written in the 128-byte
+//               swizzled K-major layout the MMA reads, 64 K elements per
+//               converted slice; each thread expands half a weight row
 //   warps 10..13 epilogue: FC1 exchanges gate rows through shared memory, applies
 //               SwiGLU and re-encodes the intermediate to NVFP4; FC2 writes bf16.
+//   warps 14..15 token converters: each thread expands half a token row (rows
+//               past the expert's end are skipped)
 // Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit).
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
@@ -43,38 +43,35 @@ using namespace sm100;
 constexpr int BMW = 128;        // weight rows per tile (MMA M)
 constexpr int BNT = 32;         // tokens per tile (MMA N)
 static_assert(BNT == 32, "the FC2 epilogue hands one token per lane");
-constexpr int BKR = 256;        // K elements per raw stage
-constexpr int BKC = 64;         // K elements per converted slice (one 128-byte swizzle atom of f16)
-constexpr int kRawStages = 4;
-constexpr int kCvtWarps = 8;
-constexpr int kThreads = 64 + 32 * kCvtWarps + 128;
+constexpr int BKR = 256;        // K elements per stage
+constexpr int BKC = 64;         // K elements per slice: one 128-byte swizzle atom of f16 tokens,
+                                // 32 tensor-memory columns of f16 weights
+constexpr int kSlices = BKR / BKC;
+// Shared-memory stages: FC1 keeps 25 KB of static shared memory (gate
+// exchange, tile prefix) and runs four, FC2 five.
+template <int kMode>
+constexpr int stages() { return kMode == 0 ? 4 : 5; }
+constexpr int kAStages = 3;     // converted weight stages in tensor memory
+constexpr int kCvtWarps = 8;    // weight converters, two per TMEM lane quarter
+constexpr int kTokWarps = 2;    // token converters
+constexpr int kThreads = 64 + 32 * kCvtWarps + 128 + 32 * kTokWarps;
+constexpr int kFirstTokWarp = 2 + kCvtWarps + 4;
 constexpr uint32_t kRawW = BMW * (BKR / 2);        // 16 KB packed weights
 constexpr uint32_t kRawWS = BMW * (BKR / 16);      // 2 KB weight scales
 constexpr uint32_t kRawX = BNT * (BKR / 2);        // 4 KB packed tokens
 constexpr uint32_t kRawXS = BNT * (BKR / 16);      // 512 B token scales
-constexpr uint32_t kRawBytes = kRawW + kRawWS + kRawX + kRawXS;
-constexpr uint32_t kRawStride = 23552;             // kRawBytes rounded up to 1024
-constexpr uint32_t kCvtW = BMW * BKC * 2;          // 16 KB
-constexpr uint32_t kCvtX = BNT * BKC * 2;          // 4 KB
-constexpr uint32_t kCvtSlice = kCvtW + kCvtX;      // 20 KB: one slice, weights then tokens
-// Converted stages.  FC2 hands two slices (128 K) to the tensor cores per stage,
-// one proxy fence and one barrier arrival per 128 K per converter warp (3
-// stages); FC1, which keeps 25 KB of static shared memory for its gate
-// exchange, runs five one-slice stages, which measured faster there than two
-// two-slice stages.
-template <int kMode>
-constexpr int slices_per_cvt() { return kMode == 0 ? 1 : 2; }
-template <int kMode>
-constexpr int cvt_stages() { return kMode == 0 ? 5 : 3; }
-template <int kMode>
-constexpr uint32_t cvt_stride() { return slices_per_cvt<kMode>() * kCvtSlice; }
-constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kTmaBytes = kRawW + kRawWS + kRawX + kRawXS;
+constexpr uint32_t kXf16Off = 23552;               // f16 token slices, 1024-byte aligned
+constexpr uint32_t kXf16Slice = BNT * BKC * 2;     // 4 KB: 32 rows x 128 B, 128-byte swizzle
+constexpr uint32_t kStageStride = kXf16Off + kSlices * kXf16Slice;
+static_assert(kTmaBytes <= kXf16Off && kXf16Off % 1024 == 0 && kStageStride % 1024 == 0, "stage layout");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAColBase = 2 * BNT;            // two fp32 accumulators of N = 32 columns come first
+constexpr uint32_t kAStageCols = kSlices * (BKC / 2);  // 128 columns: 256 f16 weights per lane
+static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "tensor memory layout");
 constexpr int kMaxE = 1024;
 template <int kMode>
-constexpr size_t dyn_smem() {
-  return 1024 + (size_t)kRawStages * kRawStride + (size_t)cvt_stages<kMode>() * cvt_stride<kMode>();
-}
-static_assert(kRawBytes <= kRawStride, "raw stage layout");
+constexpr size_t dyn_smem() { return 1024 + (size_t)stages<kMode>() * kStageStride; }
 
 enum Mode { kFc1SwiGLU = 0, kFc2 = 1 };
 
@@ -184,56 +181,35 @@ MOE_DEVICE uint4 lds128(uint32_t addr) {
   return v;
 }
 
-MOE_DEVICE uint32_t lds16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+MOE_DEVICE uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
-MOE_DEVICE void sts128(uint32_t addr, const uint4& v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-// Where one thread's half row of a 64-element K slice lives, as shared-memory
-// byte offsets fixed for the whole kernel: the row's 128-byte swizzle permutes
-// 16-byte chunks by row & 7, so the input chunk of slice s and the four output
-// chunks of the half are precomputed once.
-struct HalfRow {
-  uint32_t in_off[BKR / BKC];  // raw 16-byte chunk of slice s (half h) within the row
-  uint32_t out_off[4];         // converted chunks 4h .. 4h+3 within the row
-  uint32_t scale_off;          // this half's two scale bytes within a slice's four
-};
-
-__device__ __forceinline__ HalfRow half_row(int r, int h) {
-  HalfRow hr;
-  const int sw = r & 7;
+// One 64-element K slice of a packed weight row -> 32 f16x2 words for the
+// tensor-memory A operand (word j = elements 2j, 2j+1): two 16-byte chunks of
+// the 128-byte-swizzled raw row (chunks 2s, 2s+1, permuted by row & 7) and the
+// slice's four scale codes, one per 16 elements.
+__device__ __forceinline__ void convert_row_slice(uint32_t raw_row, uint32_t scale_row, int sw, int s,
+                                                  uint32_t (&o)[32]) {
+  const uint32_t sc4 = lds32(scale_row + 4 * s);
 #pragma unroll
-  for (int s = 0; s < BKR / BKC; s++) hr.in_off[s] = (uint32_t)(((2 * s + h) ^ sw) << 4);
+  for (int h = 0; h < 2; h++) {
+    const uint4 c = lds128(raw_row + (uint32_t)(((2 * s + h) ^ sw) << 4));
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-  for (int j = 0; j < 4; j++) hr.out_off[j] = (uint32_t)(((4 * h + j) ^ sw) << 4);
-  hr.scale_off = (uint32_t)(2 * h);
-  return hr;
-}
-
-// convert_half_row with 32-bit shared-memory addresses and precomputed swizzle
-// offsets (the form FC2 measured faster with; FC1 measured slower with it).
-__device__ __forceinline__ void convert_half_row_sh(uint32_t raw_row, uint32_t scales_row, uint32_t cvt_row, int s,
-                                                    const HalfRow& hr) {
-  const uint4 c = lds128(raw_row + hr.in_off[s]);
-  const uint32_t sc2 = lds16(scales_row + 4 * s + hr.scale_off);
-  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    for (int g = 0; g < 2; g++) {
+      const uint32_t sh = e4m3_pair_to_f16x2((sc4 >> (8 * (2 * h + g))) & 0xffu);
 #pragma unroll
-  for (int g = 0; g < 2; g++) {
-    const uint32_t sh = e4m3_pair_to_f16x2((sc2 >> (8 * g)) & 0xffu);
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-      uint4 o = e2m1x8_to_f16x8(words[2 * g + i]);
-      o.x = hmul2(o.x, sh);
-      o.y = hmul2(o.y, sh);
-      o.z = hmul2(o.z, sh);
-      o.w = hmul2(o.w, sh);
-      sts128(cvt_row + hr.out_off[2 * g + i], o);
+      for (int i = 0; i < 2; i++) {
+        const uint4 v = e2m1x8_to_f16x8(words[2 * g + i]);
+        const int j = 16 * h + 8 * g + 4 * i;
+        o[j] = hmul2(v.x, sh);
+        o[j + 1] = hmul2(v.y, sh);
+        o[j + 2] = hmul2(v.z, sh);
+        o[j + 3] = hmul2(v.w, sh);
+      }
     }
   }
 }
@@ -243,38 +219,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
                               const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xs,
                               Fp4Params p) {
-  extern __shared__ uint8_t dyn_smem[];
-  constexpr int kCvtStages = cvt_stages<kMode>();
-  constexpr int kSlicesPerCvt = slices_per_cvt<kMode>();
-  constexpr uint32_t kCvtStride = cvt_stride<kMode>();
-  __shared__ __align__(8) uint64_t s_rfull[kRawStages], s_rempty[kRawStages], s_cfull[kCvtStages],
-      s_cempty[kCvtStages], s_tfull[2], s_tempty[2], s_xbar[2], s_drain;
+  extern __shared__ uint8_t dyn_smem_buf[];
+  constexpr int kStages = stages<kMode>();
+  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_afull[kAStages], s_aempty[kAStages],
+      s_tfull[2], s_tempty[2], s_xbar[2], s_ybar[2], s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_prefix[kMaxE + 1];
   __shared__ int s_nt[kMaxE];
-  __shared__ float s_gate[2][64][BNT + 1];
+  __shared__ float s_gate[2][64][BNT + 1];  // FC1: gate rows of the tile, [row][token]
+  __shared__ float s_act[2][BNT][64 + 1];    // FC1: silu(gate) * up, [token][column]
 
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-  uint8_t* raw = smem;
-  uint8_t* cvt = smem + (size_t)kRawStages * kRawStride;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem_buf) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &s_abort;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int s = 0; s < kRawStages; s++) {
-      mbar_init(&s_rfull[s], 1);
-      mbar_init(&s_rempty[s], kCvtWarps);
+    for (int s = 0; s < kStages; s++) {
+      mbar_init(&s_full[s], 1);
+      // weight and token converters have read the packed data; the MMAs have read the f16 tokens
+      mbar_init(&s_empty[s], kCvtWarps + kTokWarps + 1);
     }
-    for (int s = 0; s < kCvtStages; s++) {
-      mbar_init(&s_cfull[s], kCvtWarps);
-      mbar_init(&s_cempty[s], 1);
+    for (int a = 0; a < kAStages; a++) {
+      mbar_init(&s_afull[a], kCvtWarps + kTokWarps);
+      mbar_init(&s_aempty[a], 1);
     }
     for (int a = 0; a < 2; a++) {
       mbar_init(&s_tfull[a], 1);
       mbar_init(&s_tempty[a], 4);
       mbar_init(&s_xbar[a], 4);
+      mbar_init(&s_ybar[a], 2);
     }
     mbar_init(&s_drain, 1);
     fence_barrier_init();
@@ -323,59 +298,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_parity[kRawStages];
-      bool issued[kRawStages];
-      for (int s = 0; s < kRawStages; s++) issued[s] = false;
+      uint32_t issued_parity[kStages];
+      bool issued[kStages];
+      for (int s = 0; s < kStages; s++) issued[s] = false;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
         const int64_t wbase = (int64_t)ti.e * p.w_rows_per_expert;
         for (int kr = 0; kr < p.nkr; kr++) {
-          if (!mbar_wait(&s_rempty[stage], phase ^ 1, abort_flag, p.status)) {
+          if (!mbar_wait(&s_empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          uint8_t* st = raw + (size_t)stage * kRawStride;
-          mbar_arrive_expect_tx(&s_rfull[stage], kRawBytes);
+          uint8_t* st = smem + (size_t)stage * kStageStride;
+          mbar_arrive_expect_tx(&s_full[stage], kTmaBytes);
           const int32_t cx = kr * (BKR / 2), cs = kr * (BKR / 16);
           if (kMode == kFc1SwiGLU) {
             const int64_t up = wbase + (int64_t)ti.mt * 64, gate = up + p.gate_offset;
-            tma_load_2d(st, &tm_w, cx, (int32_t)up, &s_rfull[stage]);
-            tma_load_2d(st + kRawW / 2, &tm_w, cx, (int32_t)gate, &s_rfull[stage]);
-            tma_load_2d(st + kRawW, &tm_ws, cs, (int32_t)up, &s_rfull[stage]);
-            tma_load_2d(st + kRawW + kRawWS / 2, &tm_ws, cs, (int32_t)gate, &s_rfull[stage]);
+            tma_load_2d(st, &tm_w, cx, (int32_t)up, &s_full[stage]);
+            tma_load_2d(st + kRawW / 2, &tm_w, cx, (int32_t)gate, &s_full[stage]);
+            tma_load_2d(st + kRawW, &tm_ws, cs, (int32_t)up, &s_full[stage]);
+            tma_load_2d(st + kRawW + kRawWS / 2, &tm_ws, cs, (int32_t)gate, &s_full[stage]);
           } else {
             const int64_t r0 = wbase + (int64_t)ti.mt * BMW;
-            tma_load_2d(st, &tm_w, cx, (int32_t)r0, &s_rfull[stage]);
-            tma_load_2d(st + kRawW, &tm_ws, cs, (int32_t)r0, &s_rfull[stage]);
+            tma_load_2d(st, &tm_w, cx, (int32_t)r0, &s_full[stage]);
+            tma_load_2d(st + kRawW, &tm_ws, cs, (int32_t)r0, &s_full[stage]);
           }
-          tma_load_2d(st + kRawW + kRawWS, &tm_x, cx, (int32_t)ti.row0, &s_rfull[stage]);
-          tma_load_2d(st + kRawW + kRawWS + kRawX, &tm_xs, cs, (int32_t)ti.row0, &s_rfull[stage]);
+          tma_load_2d(st + kRawW + kRawWS, &tm_x, cx, (int32_t)ti.row0, &s_full[stage]);
+          tma_load_2d(st + kRawW + kRawWS + kRawX, &tm_xs, cs, (int32_t)ti.row0, &s_full[stage]);
           issued[stage] = true;
           issued_parity[stage] = phase;
-          if (++stage == kRawStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
       if (!ok) {
-        for (int s = 0; s < kRawStages; s++) {
+        for (int s = 0; s < kStages; s++) {
           if (!issued[s]) continue;
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&s_rfull[s], issued_parity[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          while (!mbar_try_wait(&s_full[s], issued_parity[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // A = the converted weight stage in tensor memory, B = the f16 token slices
+    // of the same shared-memory stage.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(BMW, BNT);
-      int cst = 0, acc = 0;
-      uint32_t cphase = 0, acc_phase = 0;
+      const uint32_t smem_base = smem_u32(smem);
+      int stage = 0, ast = 0, acc = 0;
+      uint32_t aphase = 0, acc_phase = 0;
       bool ok = true;
-      const int nsub = p.nkr * (BKR / BKC) / kSlicesPerCvt;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         if (!mbar_wait(&s_tempty[acc], acc_phase ^ 1, abort_flag, p.status)) {
           ok = false;
@@ -383,26 +360,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BNT);
-        for (int ks = 0; ks < nsub; ks++) {
-          if (!mbar_wait(&s_cfull[cst], cphase, abort_flag, p.status)) {
+        for (int kr = 0; kr < p.nkr; kr++) {
+          if (!mbar_wait(&s_afull[ast], aphase, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint32_t a0 = tmem_base + kAColBase + (uint32_t)ast * kAStageCols;
+          const uint32_t x0 = smem_base + (uint32_t)stage * kStageStride + kXf16Off;
 #pragma unroll
-          for (int sl = 0; sl < kSlicesPerCvt; sl++) {
-            const uint32_t cw = smem_u32(cvt + (size_t)cst * kCvtStride + (size_t)sl * kCvtSlice);
-            const uint64_t wdesc = smem_desc_sw128(cw);
-            const uint64_t xdesc = smem_desc_sw128(cw + kCvtW);
+          for (int sl = 0; sl < kSlices; sl++) {
+            const uint64_t xdesc = smem_desc_sw128(x0 + (uint32_t)sl * kXf16Slice);
 #pragma unroll
             for (int k = 0; k < BKC / 16; k++)
-              mma_bf16(d_tmem, wdesc + 2 * k, xdesc + 2 * k, idesc, (ks | sl | k) != 0 ? 1u : 0u);
+              mma_f16_tmem_a(d_tmem, a0 + (uint32_t)(sl * (BKC / 2) + 8 * k), xdesc + 2 * k, idesc,
+                             (kr | sl | k) != 0 ? 1u : 0u);
           }
-          mma_commit(&s_cempty[cst]);
-          if (++cst == kCvtStages) {
-            cst = 0;
-            cphase ^= 1;
+          mma_commit(&s_aempty[ast]);
+          mma_commit(&s_empty[stage]);
+          if (++ast == kAStages) {
+            ast = 0;
+            aphase ^= 1;
           }
+          if (++stage == kStages) stage = 0;
         }
         if (!ok) break;
         mma_commit(&s_tfull[acc]);
@@ -419,75 +399,111 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 2 + kCvtWarps) {
-    // ---------------------------------------------------------- converters
-    const int c = threadIdx.x - 64;  // 0..255: weight row c & 127, half c >> 7
-    const int wrow = c & 127, whalf = c >> 7;
-    const int xrow = c >> 1, xhalf = c & 1;  // token half-rows for c < 64: rows 0..15 in warp 2
-    const HalfRow whr = half_row(wrow, whalf), xhr = half_row(xrow, xhalf);
-    const uint32_t raw_base = smem_u32(raw), cvt_base = smem_u32(cvt);
-    int rst = 0, cst = 0;
-    uint32_t rphase = 0, cphase = 0;
+    // ---------------------------------------------------------- weight converters
+    // Thread = weight row of the tile = TMEM lane (warp w reaches lane quarter
+    // w & 3); the two warps of a quarter take two slices each of a stage.  The
+    // converted row is stored straight into tensor memory, where the MMA reads
+    // its A operand: no shared-memory round trip and no proxy fence.
+    const int q = warp & 3, grp = (warp - 2) >> 2;
+    const int row = 32 * q + lane, sw = row & 7;
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t lane_field = (uint32_t)(32 * q) << 16;
+    int stage = 0, ast = 0;
+    uint32_t phase = 0, aphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      // Token rows past the expert's end are not converted: the accumulator
-      // column of a token row depends on that row alone, and the epilogue stores
-      // valid rows only, so whatever those columns of the converted stage hold
-      // never reaches the output.  Whole warps skip when their rows are all past it.
-      const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
-      const bool x_conv = c < 2 * BNT && (int64_t)xrow < ti.row_end - ti.row0;
-      for (int kr = 0; kr < p.nkr && ok; kr++) {
+      for (int kr = 0; kr < p.nkr; kr++) {
         int w_ok = 0;
-        if (lane == 0) w_ok = mbar_wait(&s_rfull[rst], rphase, abort_flag, p.status) ? 1 : 0;
+        if (lane == 0)
+          w_ok = (mbar_wait(&s_full[stage], phase, abort_flag, p.status) &&
+                  mbar_wait(&s_aempty[ast], aphase ^ 1, abort_flag, p.status))
+                     ? 1
+                     : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) {
           ok = false;
           break;
         }
-        const uint8_t* st = raw + (size_t)rst * kRawStride;
-        for (int s0 = 0; s0 < BKR / BKC; s0 += kSlicesPerCvt) {
-          int c_ok = 0;
-          if (lane == 0) c_ok = mbar_wait(&s_cempty[cst], cphase ^ 1, abort_flag, p.status) ? 1 : 0;
-          c_ok = __shfl_sync(0xffffffffu, c_ok, 0);
-          if (!c_ok) {
-            ok = false;
-            break;
-          }
+        tc_fence_after();
+        const uint32_t sbase = smem_base + (uint32_t)stage * kStageStride;
+        const uint32_t raw_row = sbase + (uint32_t)row * (BKR / 2);
+        const uint32_t sc_row = sbase + kRawW + (uint32_t)row * (BKR / 16);
+        const uint32_t a_cols = tmem_base + lane_field + kAColBase + (uint32_t)ast * kAStageCols;
 #pragma unroll
-          for (int sl = 0; sl < kSlicesPerCvt; sl++) {
-            const int s = s0 + sl;
-            if (kMode == kFc2) {
-              const uint32_t sts = raw_base + (uint32_t)rst * kRawStride;
-              const uint32_t cs = cvt_base + (uint32_t)cst * kCvtStride + (uint32_t)sl * kCvtSlice;
-              convert_half_row_sh(sts + wrow * (BKR / 2), sts + kRawW + wrow * (BKR / 16), cs + wrow * (BKC * 2), s,
-                                  whr);
-              if (x_conv)
-                convert_half_row_sh(sts + kRawW + kRawWS + xrow * (BKR / 2),
-                                    sts + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2),
-                                    s, xhr);
-            } else {
-              uint8_t* cs = cvt + (size_t)cst * kCvtStride + (size_t)sl * kCvtSlice;
-              convert_half_row(st + wrow * (BKR / 2), wrow, s, whalf, st + kRawW + wrow * (BKR / 16),
-                               cs + wrow * (BKC * 2));
-              if (x_conv)
-                convert_half_row(st + kRawW + kRawWS + xrow * (BKR / 2), xrow, s, xhalf,
-                                 st + kRawW + kRawWS + kRawX + xrow * (BKR / 16), cs + kCvtW + xrow * (BKC * 2));
-            }
-          }
-          // make the generic-proxy stores visible to the tensor cores, then publish
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_cfull[cst]);
-          if (++cst == kCvtStages) {
-            cst = 0;
-            cphase ^= 1;
-          }
+        for (int i = 0; i < kSlices / 2; i++) {
+          const int sl = 2 * grp + i;
+          uint32_t o[32];
+          convert_row_slice(raw_row, sc_row, sw, sl, o);
+          tmem_st32(a_cols + (uint32_t)(sl * (BKC / 2)), o);
         }
-        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_rempty[rst]);
-        if (++rst == kRawStages) {
-          rst = 0;
-          rphase ^= 1;
+        if (lane == 0) {
+          mbar_arrive(&s_afull[ast]);
+          mbar_arrive(&s_empty[stage]);
+        }
+        if (++ast == kAStages) {
+          ast = 0;
+          aphase ^= 1;
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp >= kFirstTokWarp) {
+    // ---------------------------------------------------------- token converters
+    // Thread c (0..63) expands half c & 1 of token row c >> 1 for the stage's
+    // four slices into the stage's f16 token area.  Token rows past the
+    // expert's end are not converted: the accumulator column of a token row
+    // depends on that row alone, and the epilogue stores valid rows only, so
+    // whatever those rows of the area hold never reaches the output.
+    const int c = (int)threadIdx.x - 32 * kFirstTokWarp;
+    const int row = c >> 1, half = c & 1;
+    int stage = 0, ast = 0;
+    uint32_t phase = 0, aphase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
+      const bool conv = (int64_t)row < ti.row_end - ti.row0;
+      for (int kr = 0; kr < p.nkr; kr++) {
+        // the tensor-memory stage is waited for too, so that this warp's arrival
+        // on its full barrier cannot run a phase ahead of the weight converters
+        int w_ok = 0;
+        if (lane == 0)
+          w_ok = (mbar_wait(&s_full[stage], phase, abort_flag, p.status) &&
+                  mbar_wait(&s_aempty[ast], aphase ^ 1, abort_flag, p.status))
+                     ? 1
+                     : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + (size_t)stage * kStageStride;
+        if (conv) {
+#pragma unroll
+          for (int sl = 0; sl < kSlices; sl++)
+            convert_half_row(st + kRawW + kRawWS + row * (BKR / 2), row, sl, half,
+                             st + kRawW + kRawWS + kRawX + row * (BKR / 16),
+                             st + kXf16Off + sl * kXf16Slice + row * (BKC * 2));
+        }
+        // make the generic-proxy stores visible to the tensor cores, then publish
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&s_afull[ast]);
+          mbar_arrive(&s_empty[stage]);
+        }
+        if (++ast == kAStages) {
+          ast = 0;
+          aphase ^= 1;
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
         }
       }
     }
@@ -539,40 +555,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // rows 0..63 of the tile are up (w3), rows 64..127 gate (w1) of columns mt*64 + (wr & 63)
-        float (*gbuf)[BNT + 1] = s_gate[tile_iter & 1];
+        // rows 0..63 of the tile are up (w3), rows 64..127 gate (w1) of
+        // intermediate columns mt*64 + (wr & 63).  (1) the gate rows go to shared
+        // memory; (2) the up rows form silu(gate) * up and write it token-major;
+        // (3) each thread encodes one (token, 16-column block) of it to NVFP4,
+        // all tokens of the tile in parallel.  Buffers alternate by tile and
+        // every tile passes both barriers, so a buffer is rewritten only after
+        // all four warps have finished the tile that used it before.
+        const int buf = tile_iter & 1;
+        const uint32_t bphase = (uint32_t)(tile_iter >> 1) & 1u;
+        float (*gbuf)[BNT + 1] = s_gate[buf];
+        float (*abuf)[64 + 1] = s_act[buf];
         if (q >= 2) {
 #pragma unroll
           for (int j = 0; j < BNT; j++) gbuf[wr - 64][j] = alpha * v[j];
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_xbar[tile_iter & 1]);
-        int x_ok = 0;
-        if (lane == 0) x_ok = mbar_wait(&s_xbar[tile_iter & 1], (tile_iter >> 1) & 1, abort_flag, p.status) ? 1 : 0;
-        x_ok = __shfl_sync(0xffffffffu, x_ok, 0);
-        if (!x_ok) break;
+        if (lane == 0) mbar_arrive(&s_xbar[buf]);
+        const int64_t nvalid = ti.row_end - ti.row0;  // token columns of this tile that exist
         if (q < 2) {
-          const float g2 = *p.out_global;
-          const int64_t col = (int64_t)ti.mt * 64 + wr;  // intermediate column of this thread
-          const int64_t nvalid = ti.row_end - ti.row0;    // token columns of this tile that exist
+          int x_ok = 0;
+          if (lane == 0) x_ok = mbar_wait(&s_xbar[buf], bphase, abort_flag, p.status) ? 1 : 0;
+          x_ok = __shfl_sync(0xffffffffu, x_ok, 0);
+          if (!x_ok) break;
 #pragma unroll
           for (int j = 0; j < BNT; j++) {
             if (j >= nvalid) break;  // warp-uniform
             const float gt = gbuf[wr][j];
-            const float a = gt / (1.0f + __expf(-gt)) * (alpha * v[j]);
-            // NVFP4 block = 16 consecutive columns = 16 consecutive lanes
-            float amax = fabsf(a);
-#pragma unroll
-            for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-            const uint32_t scode = e4m3x2(__fdiv_rn(amax, 6.0f * g2), 0.0f) & 0xffu;
-            const float denom = e4m3_to_float(scode) * g2;
-            const float partner = __shfl_xor_sync(0xffffffffu, a, 1);
-            const int64_t row = ti.row0 + j;
-            if ((lane & 1) == 0) {
-              const uint32_t b = (denom == 0.0f) ? 0u : e2m1x2(__fdiv_rn(a, denom), __fdiv_rn(partner, denom));
-              p.out[row * (p.ld_out / 2) + col / 2] = (uint8_t)b;
-            }
-            if ((lane & 15) == 0) p.out_scales[row * (p.ld_out / 16) + col / 16] = (uint8_t)scode;
+            abuf[j][wr] = gt / (1.0f + __expf(-gt)) * (alpha * v[j]);
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_ybar[buf]);
+        }
+        int y_ok = 0;
+        if (lane == 0) y_ok = mbar_wait(&s_ybar[buf], bphase, abort_flag, p.status) ? 1 : 0;
+        y_ok = __shfl_sync(0xffffffffu, y_ok, 0);
+        if (!y_ok) break;
+        // token j = lane, columns 16q .. 16q+15 of the tile
+        if (lane < nvalid) {
+          const float g2 = *p.out_global;
+          float a[16];
+          float amax = 0.0f;
+#pragma unroll
+          for (int c = 0; c < 16; c++) {
+            a[c] = abuf[lane][16 * q + c];
+            amax = fmaxf(amax, fabsf(a[c]));
+          }
+          const uint32_t scode = e4m3x2(__fdiv_rn(amax, 6.0f * g2), 0.0f) & 0xffu;
+          const float denom = e4m3_to_float(scode) * g2;
+          uint32_t packed[2] = {0u, 0u};
+          if (denom != 0.0f) {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+              packed[k >> 2] |= e2m1x2(__fdiv_rn(a[2 * k], denom), __fdiv_rn(a[2 * k + 1], denom)) << (8 * (k & 3));
+          }
+          const int64_t row = ti.row0 + lane;
+          const int64_t col0 = (int64_t)ti.mt * 64 + 16 * q;  // first intermediate column of the block
+          *reinterpret_cast<uint2*>(p.out + row * (p.ld_out / 2) + col0 / 2) = make_uint2(packed[0], packed[1]);
+          p.out_scales[row * (p.ld_out / 16) + col0 / 16] = (uint8_t)scode;
         }
       }
     }
