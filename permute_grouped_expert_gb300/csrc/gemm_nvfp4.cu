@@ -12,23 +12,26 @@
 // expert's tokens the N = 32 side, D^T = W . X^T, so no MMA lane is wasted on
 // the handful of rows a decode batch routes to each expert.  E2M1 x E4M3 is
 // exactly representable in f16 (at most 6 significant bits, magnitudes in
-// [2^-10, 2688]), so converter warps expand both operands to f16 in shared
-// memory exactly and tcgen05.mma kind::f16 accumulates in fp32; the two fp32
-// global scales (alpha = activation global x expert weight global) are applied
-// in the epilogue.
+// [2^-10, 2688]), so converter warps expand both operands to f16 exactly and
+// tcgen05.mma kind::f16 accumulates in fp32; the two fp32 global scales
+// (alpha = activation global x expert weight global) are applied in the
+// epilogue.  The expanded weights are stored straight into tensor memory
+// (tcgen05.st), where the MMA reads its A operand; the expanded tokens go to
+// shared memory (the B operand).
 //
 // One CTA per SM, 16 warps:
-//   warp 0      TMA producer: raw stages of 256 K elements (packed weights
-//               128 rows x 128 B, their scales 128 x 16 B, packed tokens 32 x 128 B,
-//               their scales 32 x 16 B), 4 stages
-//   warp 1      TMEM allocation (2 x 32 fp32 columns) and MMA issue
-//   warps 2..9  weight converters: E2M1 + E4M3 -> f16, written in the 128-byte
-//               swizzled K-major layout the MMA reads, 64 K elements per
-//               converted slice; each thread expands half a weight row
+//   warp 0      TMA producer: stages of 256 K elements (packed weights 128 rows
+//               x 128 B, their scales 128 x 16 B, packed tokens 32 x 128 B, their
+//               scales 32 x 16 B); 6 stages (FC1) / 7 (FC2)
+//   warp 1      TMEM allocation (512 columns: two 32-column fp32 accumulators,
+//               three 128-column f16 weight stages) and MMA issue
+//   warps 2..9  weight converters, two per TMEM lane quarter, two 64-K slices
+//               each per stage, software pipelined
 //   warps 10..13 epilogue: FC1 exchanges gate rows through shared memory, applies
-//               SwiGLU and re-encodes the intermediate to NVFP4; FC2 writes bf16.
+//               SwiGLU and encodes the intermediate to NVFP4 one (token, 16-column
+//               block) per thread; FC2 writes bf16
 //   warps 14..15 token converters: each thread expands half a token row (rows
-//               past the expert's end are skipped)
+//               past the expert's end are skipped) into a two-slot f16 ring
 // Every wait is bounded (MOE_DEV_ERR_TIMEOUT, then a clean exit).
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
@@ -47,10 +50,11 @@ constexpr int BKR = 256;        // K elements per stage
 constexpr int BKC = 64;         // K elements per slice: one 128-byte swizzle atom of f16 tokens,
                                 // 32 tensor-memory columns of f16 weights
 constexpr int kSlices = BKR / BKC;
-// Shared-memory stages: FC1 keeps 25 KB of static shared memory (gate
-// exchange, tile prefix) and runs four, FC2 five.
+// Shared-memory stages of packed weights and tokens (the bytes in flight from
+// HBM): FC1 keeps 41 KB of static shared memory (gate exchange, activation
+// transpose, tile prefix) and runs six, FC2 seven.
 template <int kMode>
-constexpr int stages() { return kMode == 0 ? 4 : 5; }
+constexpr int stages() { return kMode == 0 ? 6 : 7; }
 constexpr int kAStages = 3;     // converted weight stages in tensor memory
 constexpr int kCvtWarps = 8;    // weight converters, two per TMEM lane quarter
 constexpr int kTokWarps = 2;    // token converters
@@ -61,17 +65,18 @@ constexpr uint32_t kRawWS = BMW * (BKR / 16);      // 2 KB weight scales
 constexpr uint32_t kRawX = BNT * (BKR / 2);        // 4 KB packed tokens
 constexpr uint32_t kRawXS = BNT * (BKR / 16);      // 512 B token scales
 constexpr uint32_t kTmaBytes = kRawW + kRawWS + kRawX + kRawXS;
-constexpr uint32_t kXf16Off = 23552;               // f16 token slices, 1024-byte aligned
+constexpr uint32_t kStageStride = 23552;           // one TMA stage, rounded up to 1024 bytes
 constexpr uint32_t kXf16Slice = BNT * BKC * 2;     // 4 KB: 32 rows x 128 B, 128-byte swizzle
-constexpr uint32_t kStageStride = kXf16Off + kSlices * kXf16Slice;
-static_assert(kTmaBytes <= kXf16Off && kXf16Off % 1024 == 0 && kStageStride % 1024 == 0, "stage layout");
+constexpr uint32_t kXf16Slot = kSlices * kXf16Slice;  // f16 tokens of one stage
+constexpr int kXSlots = 2;                         // f16 token slots, a ring of their own
+static_assert(kTmaBytes <= kStageStride && kStageStride % 1024 == 0, "stage layout");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAColBase = 2 * BNT;            // two fp32 accumulators of N = 32 columns come first
 constexpr uint32_t kAStageCols = kSlices * (BKC / 2);  // 128 columns: 256 f16 weights per lane
 static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "tensor memory layout");
 constexpr int kMaxE = 1024;
 template <int kMode>
-constexpr size_t dyn_smem() { return 1024 + (size_t)stages<kMode>() * kStageStride; }
+constexpr size_t dyn_smem() { return 1024 + (size_t)stages<kMode>() * kStageStride + (size_t)kXSlots * kXf16Slot; }
 
 enum Mode { kFc1SwiGLU = 0, kFc2 = 1 };
 
@@ -175,29 +180,14 @@ __device__ __forceinline__ void convert_half_row(const uint8_t* raw_row_base, in
   }
 }
 
-MOE_DEVICE uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-MOE_DEVICE uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-// One 64-element K slice of a packed weight row -> 32 f16x2 words for the
-// tensor-memory A operand (word j = elements 2j, 2j+1): two 16-byte chunks of
-// the 128-byte-swizzled raw row (chunks 2s, 2s+1, permuted by row & 7) and the
-// slice's four scale codes, one per 16 elements.
-__device__ __forceinline__ void convert_row_slice(uint32_t raw_row, uint32_t scale_row, int sw, int s,
-                                                  uint32_t (&o)[32]) {
-  const uint32_t sc4 = lds32(scale_row + 4 * s);
+// One 64-element K slice of a packed weight row, already in registers (two
+// 16-byte chunks: elements 0..31 and 32..63; four scale codes, one per 16
+// elements) -> 32 f16x2 words for the tensor-memory A operand, word j =
+// elements 2j, 2j+1.
+__device__ __forceinline__ void convert_row_slice_regs(const uint4 (&c)[2], uint32_t sc4, uint32_t (&o)[32]) {
 #pragma unroll
   for (int h = 0; h < 2; h++) {
-    const uint4 c = lds128(raw_row + (uint32_t)(((2 * s + h) ^ sw) << 4));
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
 #pragma unroll
     for (int g = 0; g < 2; g++) {
       const uint32_t sh = e4m3_pair_to_f16x2((sc4 >> (8 * (2 * h + g))) & 0xffu);
@@ -214,6 +204,18 @@ __device__ __forceinline__ void convert_row_slice(uint32_t raw_row, uint32_t sca
   }
 }
 
+MOE_DEVICE uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+MOE_DEVICE uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t dyn_smem_buf[];
   constexpr int kStages = stages<kMode>();
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_afull[kAStages], s_aempty[kAStages],
+      s_xfree[kXSlots],
       s_tfull[2], s_tempty[2], s_xbar[2], s_ybar[2], s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -238,13 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     for (int s = 0; s < kStages; s++) {
       mbar_init(&s_full[s], 1);
-      // weight and token converters have read the packed data; the MMAs have read the f16 tokens
-      mbar_init(&s_empty[s], kCvtWarps + kTokWarps + 1);
+      mbar_init(&s_empty[s], kCvtWarps + kTokWarps);  // both converter kinds have read the packed data
     }
     for (int a = 0; a < kAStages; a++) {
       mbar_init(&s_afull[a], kCvtWarps + kTokWarps);
       mbar_init(&s_aempty[a], 1);
     }
+    for (int x = 0; x < kXSlots; x++) mbar_init(&s_xfree[x], 1);
     for (int a = 0; a < 2; a++) {
       mbar_init(&s_tfull[a], 1);
       mbar_init(&s_tempty[a], 4);
@@ -345,53 +348,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // A = the converted weight stage in tensor memory, B = the f16 token slices
-    // of the same shared-memory stage.
-    if (lane == 0) {
+    // A = the converted weight stage in tensor memory, B = the stage's f16
+    // token slot in shared memory.  The whole warp runs the loop; one elected
+    // lane issues.
+    {
+      const bool lead = elect_one_lane();
       constexpr uint32_t idesc = idesc_f16_f32(BMW, BNT);
       const uint32_t smem_base = smem_u32(smem);
-      int stage = 0, ast = 0, acc = 0;
+      int xs = 0, ast = 0, acc = 0;
       uint32_t aphase = 0, acc_phase = 0;
+      const uint32_t xbase = smem_base + (uint32_t)kStages * kStageStride;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        if (!mbar_wait(&s_tempty[acc], acc_phase ^ 1, abort_flag, p.status)) {
+        int w_ok = 0;
+        if (lane == 0) w_ok = mbar_wait(&s_tempty[acc], acc_phase ^ 1, abort_flag, p.status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BNT);
         for (int kr = 0; kr < p.nkr; kr++) {
-          if (!mbar_wait(&s_afull[ast], aphase, abort_flag, p.status)) {
+          int a_ok = 0;
+          if (lane == 0) a_ok = mbar_wait(&s_afull[ast], aphase, abort_flag, p.status) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, a_ok, 0)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a0 = tmem_base + kAColBase + (uint32_t)ast * kAStageCols;
-          const uint32_t x0 = smem_base + (uint32_t)stage * kStageStride + kXf16Off;
+          const uint32_t x0 = xbase + (uint32_t)xs * kXf16Slot;
+          if (lead) {
 #pragma unroll
-          for (int sl = 0; sl < kSlices; sl++) {
-            const uint64_t xdesc = smem_desc_sw128(x0 + (uint32_t)sl * kXf16Slice);
+            for (int sl = 0; sl < kSlices; sl++) {
+              const uint64_t xdesc = smem_desc_sw128(x0 + (uint32_t)sl * kXf16Slice);
 #pragma unroll
-            for (int k = 0; k < BKC / 16; k++)
-              mma_f16_tmem_a(d_tmem, a0 + (uint32_t)(sl * (BKC / 2) + 8 * k), xdesc + 2 * k, idesc,
-                             (kr | sl | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < BKC / 16; k++)
+                mma_f16_tmem_a(d_tmem, a0 + (uint32_t)(sl * (BKC / 2) + 8 * k), xdesc + 2 * k, idesc,
+                               (kr | sl | k) != 0 ? 1u : 0u);
+            }
+            mma_commit(&s_aempty[ast]);
+            mma_commit(&s_xfree[xs]);
           }
-          mma_commit(&s_aempty[ast]);
-          mma_commit(&s_empty[stage]);
+          __syncwarp();
           if (++ast == kAStages) {
             ast = 0;
             aphase ^= 1;
           }
-          if (++stage == kStages) stage = 0;
+          if (++xs == kXSlots) xs = 0;
         }
         if (!ok) break;
-        mma_commit(&s_tfull[acc]);
+        if (lead) mma_commit(&s_tfull[acc]);
+        __syncwarp();
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
-      if (!ok) {
+      if (!ok && lead) {
         mma_commit(&s_drain);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&s_drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
@@ -403,12 +417,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Thread = weight row of the tile = TMEM lane (warp w reaches lane quarter
     // w & 3); the two warps of a quarter take two slices each of a stage.  The
     // converted row is stored straight into tensor memory, where the MMA reads
-    // its A operand: no shared-memory round trip and no proxy fence.
+    // its A operand: no shared-memory round trip and no proxy fence.  Software
+    // pipelined: a stage's packed data is released as soon as it is in
+    // registers, and its TMEM stores complete while the next stage is loaded
+    // and converted; the stage is published after that.
     const int q = warp & 3, grp = (warp - 2) >> 2;
     const int row = 32 * q + lane, sw = row & 7;
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t lane_field = (uint32_t)(32 * q) << 16;
-    int stage = 0, ast = 0;
+    int stage = 0, ast = 0, prev_ast = -1;
     uint32_t phase = 0, aphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -428,21 +445,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sbase = smem_base + (uint32_t)stage * kStageStride;
         const uint32_t raw_row = sbase + (uint32_t)row * (BKR / 2);
         const uint32_t sc_row = sbase + kRawW + (uint32_t)row * (BKR / 16);
+        // this thread's packed data of the stage: two slices x (two 16-byte chunks, four scale codes)
+        uint4 c[2][2];
+        uint32_t sc[2];
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+          const int sl = 2 * grp + i;
+          sc[i] = lds32(sc_row + 4 * sl);
+          c[i][0] = lds128(raw_row + (uint32_t)(((2 * sl) ^ sw) << 4));
+          c[i][1] = lds128(raw_row + (uint32_t)(((2 * sl + 1) ^ sw) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[stage]);
+        uint32_t o[2][32];
+#pragma unroll
+        for (int i = 0; i < 2; i++) convert_row_slice_regs(c[i], sc[i], o[i]);
+        if (prev_ast >= 0) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_afull[prev_ast]);
+        }
         const uint32_t a_cols = tmem_base + lane_field + kAColBase + (uint32_t)ast * kAStageCols;
 #pragma unroll
-        for (int i = 0; i < kSlices / 2; i++) {
-          const int sl = 2 * grp + i;
-          uint32_t o[32];
-          convert_row_slice(raw_row, sc_row, sw, sl, o);
-          tmem_st32(a_cols + (uint32_t)(sl * (BKC / 2)), o);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&s_afull[ast]);
-          mbar_arrive(&s_empty[stage]);
-        }
+        for (int i = 0; i < 2; i++) tmem_st32(a_cols + (uint32_t)((2 * grp + i) * (BKC / 2)), o[i]);
+        prev_ast = ast;
         if (++ast == kAStages) {
           ast = 0;
           aphase ^= 1;
@@ -453,17 +480,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    tmem_wait_st();
+    if (ok && prev_ast >= 0) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_afull[prev_ast]);
+    }
   } else if (warp >= kFirstTokWarp) {
     // ---------------------------------------------------------- token converters
     // Thread c (0..63) expands half c & 1 of token row c >> 1 for the stage's
-    // four slices into the stage's f16 token area.  Token rows past the
+    // four slices into the next f16 token slot.  Token rows past the
     // expert's end are not converted: the accumulator column of a token row
     // depends on that row alone, and the epilogue stores valid rows only, so
     // whatever those rows of the area hold never reaches the output.
     const int c = (int)threadIdx.x - 32 * kFirstTokWarp;
     const int row = c >> 1, half = c & 1;
-    int stage = 0, ast = 0;
-    uint32_t phase = 0, aphase = 0;
+    uint8_t* xslots = smem + (size_t)kStages * kStageStride;
+    int stage = 0, ast = 0, xs = 0;
+    uint32_t phase = 0, aphase = 0, xphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
@@ -474,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int w_ok = 0;
         if (lane == 0)
           w_ok = (mbar_wait(&s_full[stage], phase, abort_flag, p.status) &&
-                  mbar_wait(&s_aempty[ast], aphase ^ 1, abort_flag, p.status))
+                  mbar_wait(&s_aempty[ast], aphase ^ 1, abort_flag, p.status) &&
+                  mbar_wait(&s_xfree[xs], xphase ^ 1, abort_flag, p.status))
                      ? 1
                      : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -482,13 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* st = smem + (size_t)stage * kStageStride;
+        const uint8_t* st = smem + (size_t)stage * kStageStride;
+        uint8_t* xslot = xslots + (size_t)xs * kXf16Slot;
         if (conv) {
 #pragma unroll
           for (int sl = 0; sl < kSlices; sl++)
             convert_half_row(st + kRawW + kRawWS + row * (BKR / 2), row, sl, half,
                              st + kRawW + kRawWS + kRawX + row * (BKR / 16),
-                             st + kXf16Off + sl * kXf16Slice + row * (BKC * 2));
+                             xslot + sl * kXf16Slice + row * (BKC * 2));
         }
         // make the generic-proxy stores visible to the tensor cores, then publish
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -500,6 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++ast == kAStages) {
           ast = 0;
           aphase ^= 1;
+        }
+        if (++xs == kXSlots) {
+          xs = 0;
+          xphase ^= 1;
         }
         if (++stage == kStages) {
           stage = 0;

@@ -82,6 +82,20 @@ MOE_DEVICE bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* ab
   }
 }
 
+// True in exactly one lane of the converged warp.  MMA issue loops run on
+// the whole warp with warp-uniform operands and issue from the elected lane:
+// the descriptors then stay in uniform registers, where a loop guarded by
+// lane == 0 has to move every operand into them before each MMA.
+MOE_DEVICE bool elect_one_lane() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ----------------------------------------------------------------------- TMA
 
 MOE_DEVICE void tma_prefetch_desc(const CUtensorMap* map) {
