@@ -132,6 +132,96 @@ __global__ void __launch_bounds__(kThreads) combine_backward_kernel(CombineBwdPa
   }
 }
 
+// The same results for hidden sizes up to 2048 (a gradient row fits in four
+// or eight 16-byte registers a lane): one warp per token, whose gradient row is read
+// from HBM once and kept in registers for all K routes, instead of once per
+// route through L2.  The expert rows of two routes are loaded before either
+// is processed, so two routes' loads are in flight at a time; each route's
+// rounding and dot-product order are those of combine_backward_kernel.
+template <int kTokVec>  // 16-byte vectors a lane holds: H <= 32 * kTokVec * 8
+__device__ __forceinline__ void load_route(const CombineBwdParams& p, int64_t nvec, int lane, int32_t r,
+                                           uint4 (&o)[kTokVec]) {
+  const uint8_t* orow = p.o + (int64_t)r * nvec * 16;
+#pragma unroll
+  for (int u = 0; u < kTokVec; u++) {
+    const int64_t idx = u * 32 + lane;
+    if (idx < nvec) o[u] = ld_stream(orow + idx * 16);
+  }
+}
+
+template <int kTokVec>
+__device__ __forceinline__ void finish_route(const CombineBwdParams& p, int64_t nvec, int lane, int32_t r, float w,
+                                             const uint4 (&g)[kTokVec], const uint4 (&o)[kTokVec], bool want_dot) {
+  uint8_t* drow = p.g_o + (int64_t)r * nvec * 16;
+  float dot = 0.0f;
+#pragma unroll
+  for (int u = 0; u < kTokVec; u++) {
+    const int64_t idx = u * 32 + lane;
+    if (idx < nvec) {
+      st_vec(drow + idx * 16, make_uint4(scale_pair(w, g[u].x), scale_pair(w, g[u].y), scale_pair(w, g[u].z),
+                                         scale_pair(w, g[u].w)));
+      if (want_dot) {
+        dot = dot_pair(g[u].x, o[u].x, dot);
+        dot = dot_pair(g[u].y, o[u].y, dot);
+        dot = dot_pair(g[u].z, o[u].z, dot);
+        dot = dot_pair(g[u].w, o[u].w, dot);
+      }
+    }
+  }
+  if (want_dot) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, d);
+    if (lane == 0) p.g_w[r] = dot;
+  }
+}
+
+template <int kTokVec>
+__global__ void __launch_bounds__(kThreads, kTokVec == 4 ? 3 : 2) combine_backward_token_kernel(CombineBwdParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nvec = p.H / 8;
+  const int64_t items = p.T + p.E;
+  const bool want_dot = p.g_w != nullptr;
+  for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
+    if (it >= p.T) {
+      // pad rows of expert e: zero gradient rows and zero probability gradients
+      const int64_t e = it - p.T;
+      const int64_t beg = (int64_t)p.offsets[e] + p.counts[e];
+      const int64_t end = min64(p.offsets[e + 1], p.cap);
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int64_t r = beg; r < end; r++) {
+        for (int64_t v = lane; v < nvec; v += 32) st_vec(p.g_o + (r * nvec + v) * 16, z);
+        if (p.g_w && lane == 0) p.g_w[r] = 0.0f;
+      }
+      continue;
+    }
+    const int64_t t = it;
+    uint4 g[kTokVec];
+#pragma unroll
+    for (int u = 0; u < kTokVec; u++) {
+      const int64_t idx = u * 32 + lane;
+      if (idx < nvec) g[u] = ld_stream(p.gy + (t * nvec + idx) * 16);
+    }
+    for (int64_t k0 = 0; k0 < p.K; k0 += 32) {
+      // lane j holds route k0 + j: its row and weight
+      const int64_t kk = k0 + lane;
+      const int32_t rr = kk < p.K ? p.row_of[t * p.K + kk] : -1;
+      const float ww = rr >= 0 && p.perm_probs ? p.perm_probs[rr] : 1.0f;
+      const int n = (int)min64(32, p.K - k0);
+      for (int j = 0; j < n; j += 2) {
+        const int32_t r0 = __shfl_sync(0xffffffffu, rr, j);
+        const float w0 = __shfl_sync(0xffffffffu, ww, j);
+        const int32_t r1 = j + 1 < n ? __shfl_sync(0xffffffffu, rr, j + 1) : -1;
+        const float w1 = __shfl_sync(0xffffffffu, ww, (j + 1) & 31);
+        uint4 o0[kTokVec], o1[kTokVec];
+        if (want_dot && r0 >= 0) load_route(p, nvec, lane, r0, o0);  // warp-uniform conditions
+        if (want_dot && r1 >= 0) load_route(p, nvec, lane, r1, o1);
+        if (r0 >= 0) finish_route(p, nvec, lane, r0, w0, g, o0, want_dot);
+        if (r1 >= 0) finish_route(p, nvec, lane, r1, w1, g, o1, want_dot);
+      }
+    }
+  }
+}
+
 struct ProbGradParams {
   int format;
   int64_t T, E, K;
@@ -196,7 +286,12 @@ cudaError_t launch_combine_backward(const moe_handle_dev& h, const moe_shape& s,
   p.perm_probs = perm_probs;
   p.g_o = static_cast<uint8_t*>(grad_expert_out);
   p.g_w = grad_perm_probs;
-  combine_backward_kernel<<<grid_for_warps(s.T * s.K + s.E), kThreads, 0, st>>>(p);
+  if (s.H <= 32 * 4 * 8)
+    combine_backward_token_kernel<4><<<grid_for_warps(s.T + s.E), kThreads, 0, st>>>(p);
+  else if (s.H <= 32 * 8 * 8)
+    combine_backward_token_kernel<8><<<grid_for_warps(s.T + s.E), kThreads, 0, st>>>(p);
+  else
+    combine_backward_kernel<<<grid_for_warps(s.T * s.K + s.E), kThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 

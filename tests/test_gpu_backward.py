@@ -44,6 +44,12 @@ CASES = [
     ("dense_overflow", workloads.scaled(workloads.WORKLOADS["permute"], T=400, H=256, E=8, K=3), "dense", 0.5),
     ("sparse_overflow", workloads.scaled(workloads.WORKLOADS["mid"], T=300, H=128, E=10, K=4), "sparse", 0.6),
     ("zero_tokens", workloads.scaled(workloads.WORKLOADS["permute"], T=0, H=128, E=4, K=2), "dense", None),
+    # hidden sizes at and past the token-per-warp kernels' register rows (1024, 2048) and the route-per-warp
+    # kernel beyond; top-36 takes the token kernel through a second 32-route pass
+    ("h1024_top36", workloads.scaled(workloads.WORKLOADS["stress"], T=200, H=1024, E=64, K=36), "dense", None),
+    ("h1152_sparse", workloads.scaled(workloads.WORKLOADS["mid"], T=257, H=1152, E=16, K=4), "sparse", None),
+    ("h2048_overflow", workloads.scaled(workloads.WORKLOADS["mid"], T=300, H=2048, E=16, K=8), "sparse", 0.7),
+    ("h2176", workloads.scaled(workloads.WORKLOADS["permute"], T=130, H=2176, E=8, K=3), "dense", None),
 ]
 
 
