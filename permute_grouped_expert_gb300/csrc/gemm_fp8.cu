@@ -92,16 +92,6 @@ MOE_DEVICE void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 
-// x / s from the reciprocal rs = RN(1/s): one product and one FMA correction
-// step (P. Markstein, "Computation of elementary functions on the IBM RISC
-// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  The intermediate's
-// FP8 encoding divides 64 values a thread by one scale; this replaces 64 IEEE
-// divisions with one reciprocal and three instructions each.
-MOE_DEVICE float div_by_scale(float x, float s, float rs) {
-  const float q = x * rs;
-  return fmaf(fmaf(-q, s, x), rs, q);
-}
-
 struct Fp8Params {
   const int32_t* offsets;    // [E+1]
   int32_t* status;

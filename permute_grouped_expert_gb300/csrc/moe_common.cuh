@@ -67,6 +67,18 @@ MOE_DEVICE uint32_t float_to_bf16_bits(float f) {
   return (uint32_t)(*reinterpret_cast<unsigned short*>(&h));
 }
 
+// x / s from the reciprocal rs = RN(1/s): one product and one FMA correction
+// step (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  For a 1x128 FP8
+// block scale s = RN(amax / 448) and |x| <= amax it equals the correctly
+// rounded quotient, i.e. an IEEE division; the FP8 encoders divide a block's
+// values by one scale, so one reciprocal and three instructions replace a
+// division per value.
+MOE_DEVICE float div_by_scale(float x, float s, float rs) {
+  const float q = x * rs;
+  return fmaf(fmaf(-q, s, x), rs, q);
+}
+
 // Two fp32 -> E4M3 codes, nearest even, saturating (low byte = a).
 MOE_DEVICE uint16_t e4m3x2(float a, float b) {
   uint16_t r;

@@ -168,33 +168,37 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchParams p
     load_dests(p, soff, t, s_dest[warp], chunk == 0);
     const uint8_t* src = p.x + t * H * 2;
     const int64_t chunk_end = min64(H, (chunk + 1) * kChunk);
-    for (int64_t base = chunk * kChunk; base < chunk_end; base += 256 * 2) {
-      uint2 q[2];
+    // each lane encodes 16 consecutive elements (one 16-byte code store a
+    // destination); eight lanes share a 128-element scale block
+    for (int64_t base = chunk * kChunk; base < chunk_end; base += 512 * 2) {
+      uint4 q[2];
       float sc[2];
       bool live[2];
 #pragma unroll
       for (int u = 0; u < 2; u++) {
-        const int64_t e0 = base + u * 256 + lane * 8;
-        live[u] = e0 < chunk_end;  // H and the chunk are multiples of 128: a 16-lane block is live or dead as a whole
-        uint4 v = live[u] ? ld_stream(src + e0 * 2) : make_uint4(0, 0, 0, 0);
-        float f[8];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const int64_t e0 = base + u * 512 + lane * 16;
+        live[u] = e0 < chunk_end;  // H and the chunk are multiples of 128: an 8-lane block is live or dead as a whole
+        const uint4 v0 = live[u] ? ld_stream(src + e0 * 2) : make_uint4(0, 0, 0, 0);
+        const uint4 v1 = live[u] ? ld_stream(src + e0 * 2 + 16) : make_uint4(0, 0, 0, 0);
+        float f[16];
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
+        for (int j = 0; j < 8; j++) {
           f[2 * j] = bf16_bits_to_float(w[j] & 0xffffu);
           f[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
         }
         float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(f[j]));
+        for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
 #pragma unroll
-        for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        for (int d = 4; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
         const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+        const float rs = __frcp_rn(s);
         sc[u] = s;
-        uint32_t c[4];
+        uint32_t c[8];
 #pragma unroll
-        for (int j = 0; j < 4; j++) c[j] = e4m3x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
-        q[u] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+        for (int j = 0; j < 8; j++) c[j] = e4m3x2(div_by_scale(f[2 * j], s, rs), div_by_scale(f[2 * j + 1], s, rs));
+        q[u] = make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
       }
       for (int k = 0; k < p.K; k++) {
         const int32_t d = s_dest[warp][k];
@@ -204,9 +208,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchParams p
 #pragma unroll
         for (int u = 0; u < 2; u++) {
           if (!live[u]) continue;
-          const int64_t e0 = base + u * 256 + lane * 8;
-          *reinterpret_cast<uint2*>(dst + e0) = q[u];
-          if ((lane & 15) == 0) sdst[e0 / 128] = sc[u];
+          const int64_t e0 = base + u * 512 + lane * 16;
+          st_vec(dst + e0, q[u]);
+          if ((lane & 7) == 0) sdst[e0 / 128] = sc[u];
         }
       }
     }

@@ -1,6 +1,7 @@
-"""The FP8 grouped GEMM encodes its intermediate with x / s computed from the
-reciprocal rs = RN(1/s) as q = RN(x * rs), then q + RN(x - q*s) * rs rounded
-once (Markstein's correction step; the residual is exact under fma).  Emulated
+"""The FP8 grouped GEMM encodes its intermediate, and the FP8 dispatch its
+token rows, with x / s computed from the reciprocal rs = RN(1/s) as
+q = RN(x * rs), then q + RN(x - q*s) * rs rounded once (Markstein's correction
+step; the residual is exact under fma).  Emulated
 here with exact rational arithmetic on fp32 inputs: over the range the kernel
 uses (s = amax / 448, |x| <= amax) the result equals the correctly rounded
 fp32 quotient, i.e. what an IEEE division gives."""
