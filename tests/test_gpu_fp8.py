@@ -138,3 +138,33 @@ def test_dsv3_layer_full_size_sampled(oracle, moe):
     o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"][toks], po)
     assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"][torch.from_numpy(toks).cuda()])),
                          oracle.bf16_to_f64(yref), o_rows, wts) <= TOL_FP8
+
+
+def test_fp8_overflowed_capacity(oracle, moe):
+    """Capacity at half the padded rows (4-aligned, cutting an expert segment
+    inside a token tile): the kept rows match the oracle, pad rows are zero,
+    rows at or past the capacity's end of the segments are never written, and
+    dropped routes contribute nothing to the layer."""
+    w = _case(T=256, H=512, E=8, K=2, I=256)
+    fmt, rmap, _ = workloads.routing_inputs(w, 63)
+    total = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, 1 << 30)["total_rows"]
+    cap = oracle.capacity(total // 2 + 6, 1.0)
+    r = run_layer_fp8(moe, w, seed=63, cap=cap)
+    pre = oracle.preprocess(r["fmt"], r["rmap"], w.T, w.E, w.K, w.m, cap)
+    assert pre["overflow"] == 1 and cap % 32 != 0
+    v = pre["valid_rows"]
+    rows = np.arange(v)[pre["token_of"] >= 0]
+    sel, ob = _oracle_rows(oracle, w, r, rows, pre)
+    got = bits(r["o"][torch.from_numpy(sel).cuda()])
+    assert rel_err(oracle.bf16_to_f64(got), oracle.bf16_to_f64(ob)) <= TOL_FP8
+    o_all = bits(r["o"])
+    for e in range(w.E):
+        for row in range(pre["offsets"][e] + pre["counts"][e], min(pre["offsets"][e + 1], cap)):
+            assert not o_all[row].any()
+    assert np.all(o_all[v:] == 0xFFFF)
+    _, po = oracle.dispatch(r["fmt"], r["rmap"], r["probs"], pre, np.zeros((w.T, 1), np.uint8), cap, w.E, w.K)
+    o_full = np.zeros((cap, w.H), np.uint16)
+    o_full[sel] = ob
+    yref = oracle.combine(o_full, pre["row_of"], po)
+    o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"], po)
+    assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"])), oracle.bf16_to_f64(yref), o_rows, wts) <= TOL_FP8

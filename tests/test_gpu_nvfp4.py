@@ -32,9 +32,9 @@ def _globals(x, w13, w2):
     return gx, g13, g2
 
 
-def run_layer_nvfp4(moe, w, seed):
+def run_layer_nvfp4(moe, w, seed, cap=None):
     fmt, rmap, probs = workloads.routing_inputs(w, seed)
-    cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
+    cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m) if cap is None else cap
     x = workloads.activations(w, seed)
     w13, w2 = workloads.expert_weights(w, seed, device="cuda")
     gx, g13, g2 = _globals(x, w13, w2)
@@ -157,3 +157,21 @@ def test_decode_full_size(oracle, moe, name, n_tokens):
     o_rows, wts = gather_rows(oracle.bf16_to_f64(o_full), pre["row_of"][toks], po)
     assert layer_rel_err(oracle.bf16_to_f64(bits(r["out"][torch.from_numpy(toks).cuda()])),
                          oracle.bf16_to_f64(yref), o_rows, wts) <= TOL_FP4
+
+
+def test_nvfp4_overflowed_capacity(oracle, moe):
+    """Capacity at half the padded rows, cutting an expert segment inside a
+    token tile: kept routes match the oracle (rows and layer), pad rows are
+    zero and rows past the capacity's end of the segments are never written."""
+    w = _case(T=160, H=512, E=6, K=3, I=256)
+    fmt, rmap, _ = workloads.routing_inputs(w, 73)
+    total = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, 1 << 30)["total_rows"]
+    cap = oracle.capacity(total // 2 + 6, 1.0)
+    r = run_layer_nvfp4(moe, w, seed=73, cap=cap)
+    pre = _check(oracle, w, r, np.arange(w.T))
+    assert pre["overflow"] == 1 and cap % 32 != 0
+    o_all = bits(r["o"])
+    for e in range(w.E):
+        for row in range(pre["offsets"][e] + pre["counts"][e], min(pre["offsets"][e + 1], cap)):
+            assert not o_all[row].any()
+    assert np.all(o_all[pre["valid_rows"]:] == 0xFFFF)
