@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -105,7 +106,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -116,11 +117,26 @@ class ClockSampler:
                 smax.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": round(statistics.median(power), 1) if power else None}
+
+
+PRE_ROLL_S = 0.5  # seconds of warm replays between the clock sampler's start and a timed region
+
+
+def pre_roll_count(step_ms: float, minimum: int) -> int:
+    """Warm replays that keep the GPU busy for PRE_ROLL_S after the clock sampler
+    starts (its first sample comes 0.1-0.2 s later), so that the samples fall
+    under load; at least `minimum`."""
+    return max(minimum, int(math.ceil(PRE_ROLL_S * 1e3 / max(step_ms, 1e-3))))
 
 
 # ------------------------------------------------------- multi-rank timing
@@ -451,11 +467,17 @@ def run_ours(args, w):
         dist.barrier()
     torch.cuda.synchronize()
     step_evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    est = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    with torch.cuda.stream(stream):
+        est[0].record(stream)
+        replay_step(graphs, 0, stream, None)
+        est[1].record(stream)
+    torch.cuda.synchronize()
+    n_pre = pre_roll_count(est[0].elapsed_time(est[1]), W)
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     clocks.start()
-    time.sleep(0.3)
     with torch.cuda.stream(stream):
-        for _ in range(W):  # warm replays of the captured graphs
+        for _ in range(n_pre):  # warm replays of the captured graphs, under the clock sampler
             replay_step(graphs, 0, stream, None)
         for i in range(K):
             step_evs[i].record(stream)
@@ -522,6 +544,11 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    e2e_clocks = ClockSampler(clocks.gpu)
+    e2e_clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(n_pre):  # load under the sampler's first samples
+            replay_step(graphs, 0, stream, None)
     e2e_evs[0].record(stream)
     cin.wait_event(e2e_evs[0])
     for i in range(K):
@@ -548,6 +575,7 @@ def run_ours(args, w):
     stream.wait_event(last_out)
     e2e_evs[1].record(stream)
     torch.cuda.synchronize()
+    e2e_clk = e2e_clocks.stop()
     e2e_ms = max_over_ranks(e2e_evs[0].elapsed_time(e2e_evs[1]), dev)
 
     R = prob.routed_rows()
@@ -657,7 +685,7 @@ def run_ours(args, w):
         "roofline": roof,
         "breakdown": breakdown,
         "e2e": {"value": round(job_throughput(w.T, world, K, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5), "clocks": e2e_clk},
         "gpu_launches": prob.kernels_per_step() * K,
         "clocks": clk,
     }
@@ -793,11 +821,18 @@ def run_backward(args, w):
     end = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
+    est = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    with torch.cuda.stream(stream):
+        est[0].record(stream)
+        graphs[0].replay()
+        graphs[1].replay()
+        est[1].record(stream)
+    torch.cuda.synchronize()
+    n_pre = pre_roll_count(est[0].elapsed_time(est[1]), W)
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     clocks.start()
-    time.sleep(0.3)
     with torch.cuda.stream(stream):
-        for _ in range(W):
+        for _ in range(n_pre):  # warm replays under the clock sampler
             graphs[0].replay()
             graphs[1].replay()
         for i in range(K):
@@ -827,6 +862,12 @@ def run_backward(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    e2e_clocks = ClockSampler(clocks.gpu)
+    e2e_clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(n_pre):  # load under the sampler's first samples
+            graphs[0].replay()
+            graphs[1].replay()
     e0.record(stream)
     cin.wait_event(e0)
     for i in range(K):
@@ -852,6 +893,7 @@ def run_backward(args, w):
     stream.wait_event(last_out)
     e1.record(stream)
     torch.cuda.synchronize()
+    e2e_clk = e2e_clocks.stop()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
 
     R = prob.routed_rows()
@@ -895,7 +937,8 @@ def run_backward(args, w):
                       "timing": "each step two CUDA graph replays (combine backward, dispatch backward) with "
                                 "events between them"},
         "e2e": {"value": round(job_throughput(w.T, world, K, e2e_ms), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5),
+                "clocks": e2e_clk},
         "gpu_launches": bp.kernels_per_step * K,
         "clocks": clk,
     }
