@@ -127,6 +127,9 @@ enum {
                                          the extra ones are ignored */
 #define MOE_DEV_ERR_TIMEOUT 4         /* a bounded inter-CTA wait gave up; outputs of
                                          that call are not valid */
+#define MOE_DEV_ERR_BOUNDS 8          /* bounds-checked build only (compiled with
+                                         -DMOE_CHECKED): a computed index failed its
+                                         check and the access was skipped */
 
 typedef struct moe_shape {
   int64_t T; /* tokens (>= 0) */
@@ -383,6 +386,8 @@ typedef struct moe_nvfp4_globals {
  *   MOE_DTYPE_NVFP4 (perm_tokens packed [cap][H/2] + perm_scales E4M3 [cap][H/16];
  *   w13 packed [E][2I][H/2] + E4M3 [E][2I][H/16]; w2 packed [E][H][I/2] + E4M3
  *   [E][H][I/16]; globals required).
+ * Shapes: H and I multiples of 128 (MOE_ERR_INVALID_ARG otherwise); NVFP4 also
+ * needs H and I multiples of 256 (MOE_ERR_UNSUPPORTED otherwise).
  * workspace: device, >= moe_grouped_mlp_workspace_size bytes, 256-byte aligned.
  * out_fc2: device bf16 [cap][H]. */
 MOE_API moe_status moe_grouped_mlp(const moe_handle_dev* handle, const moe_shape* shape, const moe_layout* layout,

@@ -40,15 +40,26 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+FLAGS_FILE = os.path.join(BUILD, "libmoe_gb300.flags")
+
+
+def _built_flags() -> str:
+    try:
+        return open(FLAGS_FILE).read()
+    except OSError:
+        return ""
+
+
+def up_to_date(extra_flags=()) -> bool:
+    """The library exists, is newer than every source, and was built with these extra flags."""
+    if not os.path.exists(LIB) or _built_flags() != " ".join(extra_flags):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
+    if not force and up_to_date(extra_flags):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -71,8 +82,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(FLAGS_FILE, "w") as f:
+        f.write(" ".join(extra_flags))
     return LIB
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    # --checked: the bounds-checked build (-DMOE_CHECKED), a debugging build
+    # whose kernels check computed indices before they access memory
+    flags = ["-DMOE_CHECKED"] if "--checked" in sys.argv else []
+    print(build(force="--force" in sys.argv or bool(flags), verbose=True, extra_flags=flags))

@@ -471,7 +471,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         amax = fmaxf(s_amax[tile_iter & 1][0][r_local], s_amax[tile_iter & 1][1][r_local]);
         const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
         const float rs = __frcp_rn(s);
-        if (valid) {
+        if (valid && MOE_IN_BOUNDS(61, row, p.cap, p.status) &&
+            MOE_IN_BOUNDS(62, (int64_t)ti.n * 128 + 64 * grp + 63, p.ld_out, p.status)) {
           uint8_t* dst = p.out + row * p.ld_out + (int64_t)ti.n * 128 + 64 * grp;
 #pragma unroll
           for (int q = 0; q < 4; q++) {
@@ -491,7 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // each with its E8M0 scale; x / 2^X is exact in fp32, then rounded
         // to the element format (nearest even, saturating)
         const int64_t col0 = (int64_t)ti.n * BN + grp * 128;
-        if (valid && col0 < p.out_cols) {
+        if (valid && col0 < p.out_cols && MOE_IN_BOUNDS(63, row, p.cap, p.status)) {
           const bool fp8 = p.out_format == MOE_COMBINE_MXFP8;
           uint32_t sc4 = 0;
 #pragma unroll
@@ -528,7 +529,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       } else {
         const int64_t col0 = (int64_t)ti.n * BN + grp * 128;
-        if (valid && col0 < p.out_cols) {
+        if (valid && col0 < p.out_cols && MOE_IN_BOUNDS(64, row, p.cap, p.status) &&
+            MOE_IN_BOUNDS(65, col0 + 127, p.ld_out, p.status)) {
           uint8_t* dst = p.out + (row * p.ld_out + col0) * 2;
 #pragma unroll
           for (int q = 0; q < 16; q++) {

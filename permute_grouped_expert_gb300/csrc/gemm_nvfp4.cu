@@ -146,8 +146,9 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
   TileInfo ti;
   ti.e = lo;
   const int local = t - prefix[lo];
-  ti.mt = local / ntt[lo];
-  ti.nt = local % ntt[lo];
+  const int n_tok = MOE_IN_BOUNDS(31, ntt[lo] - 1, 1 << 30, p.status) ? ntt[lo] : 1;  // >= 1 token tile
+  ti.mt = local / n_tok;
+  ti.nt = local % n_tok;
   const int64_t seg_b = min64(p.offsets[lo], p.cap);
   ti.row_end = min64(p.offsets[lo + 1], p.cap);
   ti.row0 = seg_b + (int64_t)ti.nt * BNT;
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(t, s_prefix, s_nt, p);
+        (void)MOE_IN_BOUNDS(32, ti.row0, p.cap, p.status);  // a tile starts inside the capacity
         const int64_t wbase = (int64_t)ti.e * p.w_rows_per_expert;
         for (int kr = 0; kr < p.nkr; kr++) {
           if (!mbar_wait(&s_empty[stage], phase ^ 1, abort_flag, p.status)) {
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_f16_f32(BMW, BNT);
       const uint32_t smem_base = smem_u32(smem);
       int xs = 0, ast = 0, acc = 0;
-      uint32_t aphase = 0, acc_phase = 0;
+      uint32_t aphase = 0, xphase = 0, acc_phase = 0;
       const uint32_t xbase = smem_base + (uint32_t)kStages * kStageStride;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -395,7 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ast = 0;
             aphase ^= 1;
           }
-          if (++xs == kXSlots) xs = 0;
+          if (++xs == kXSlots) {
+            xs = 0;
+            xphase ^= 1;
+          }
         }
         if (!ok) break;
         if (lead) mma_commit(&s_tfull[acc]);
@@ -409,6 +414,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&s_drain);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&s_drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+      if (ok && lane == 0) {
+        // the releases of the last weight stages and token slots are mbarrier
+        // arrivals made when their MMAs complete: all of them land on this
+        // CTA's barriers before it leaves (the same waits a next stage would make)
+        for (int i = 0; i < kAStages && ok; i++) {
+          ok = mbar_wait(&s_aempty[ast], aphase ^ 1, abort_flag, p.status);
+          if (++ast == kAStages) {
+            ast = 0;
+            aphase ^= 1;
+          }
+        }
+        for (int i = 0; i < kXSlots && ok; i++) {
+          ok = mbar_wait(&s_xfree[xs], xphase ^ 1, abort_flag, p.status);
+          if (++xs == kXSlots) {
+            xs = 0;
+            xphase ^= 1;
+          }
         }
       }
     }
@@ -468,7 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t a_cols = tmem_base + lane_field + kAColBase + (uint32_t)ast * kAStageCols;
 #pragma unroll
-        for (int i = 0; i < 2; i++) tmem_st32(a_cols + (uint32_t)((2 * grp + i) * (BKC / 2)), o[i]);
+        for (int i = 0; i < 2; i++)
+          if (MOE_IN_BOUNDS(41, kAColBase + ast * kAStageCols + (2 * grp + i + 1) * (BKC / 2) - 1, kTmemCols,
+                            p.status))
+            tmem_st32(a_cols + (uint32_t)((2 * grp + i) * (BKC / 2)), o[i]);
         prev_ast = ast;
         if (++ast == kAStages) {
           ast = 0;
@@ -578,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc = 0;
         acc_phase ^= 1;
       }
-      const float alpha = xg * p.w_global[ti.e];
+      const float alpha = MOE_IN_BOUNDS(13, ti.e, p.E, p.status) ? xg * p.w_global[ti.e] : 0.0f;
       if (kMode == kFc2) {
         const int64_t col = (int64_t)ti.mt * BMW + wr;
         uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
@@ -591,7 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < BNT; j++) {
           const int64_t row = ti.row0 + j;
-          if (row < ti.row_end) out[row * p.ld_out + col] = (uint16_t)float_to_bf16_bits(alpha * v[j]);
+          if (row < ti.row_end && MOE_IN_BOUNDS(21, row, p.cap, p.status) &&
+              MOE_IN_BOUNDS(22, col, p.ld_out, p.status))
+            out[row * p.ld_out + col] = (uint16_t)float_to_bf16_bits(alpha * v[j]);
         }
       } else {
         // rows 0..63 of the tile are up (w3), rows 64..127 gate (w1) of columns mt*64 + (wr & 63)
@@ -651,8 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int64_t row = ti.row0 + lane;
           const int64_t col0 = (int64_t)ti.mt * 64 + 16 * q;  // first intermediate column of the block
-          *reinterpret_cast<uint2*>(p.out + row * (p.ld_out / 2) + col0 / 2) = make_uint2(packed[0], packed[1]);
-          p.out_scales[row * (p.ld_out / 16) + col0 / 16] = (uint8_t)scode;
+          if (MOE_IN_BOUNDS(11, row, p.cap, p.status) && MOE_IN_BOUNDS(12, col0 + 15, p.ld_out, p.status)) {
+            *reinterpret_cast<uint2*>(p.out + row * (p.ld_out / 2) + col0 / 2) = make_uint2(packed[0], packed[1]);
+            p.out_scales[row * (p.ld_out / 16) + col0 / 16] = (uint8_t)scode;
+          }
         }
       }
     }

@@ -380,6 +380,8 @@ moe_status moe_grouped_mlp_ex(const moe_handle_dev* handle, const moe_shape* sha
       if (!perm_scales || !w13_scales || !w2_scales || !globals || !globals->fc1_input_scale ||
           !globals->fc2_input_scale || !globals->w13_scale_2 || !globals->w2_scale_2)
         return MOE_ERR_INVALID_ARG;
+      // the NVFP4 kernels stage 256 K elements at a time (FC1: K = H, FC2: K = I)
+      if (shape->H % 256 != 0 || shape->I % 256 != 0) return MOE_ERR_UNSUPPORTED;
       break;
     default:
       return MOE_ERR_INVALID_ARG;

@@ -2,6 +2,8 @@
 // library: bounded waits, acquire/release accesses, bf16 / FP8 / FP4 packing.
 #pragma once
 
+#include <cstdio>
+
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -39,6 +41,27 @@ MOE_DEVICE int32_t ld_acquire_s32(const int32_t* p) {
 MOE_DEVICE void set_status(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
+
+// Bounds-checked build (-DMOE_CHECKED): MOE_IN_BOUNDS(site, index, limit,
+// status) guards a computed index before the access it feeds; a failed check
+// sets MOE_DEV_ERR_BOUNDS, prints the site, index and limit (the first few
+// failures of a translation unit) and returns false so the caller skips the
+// access.  In the ordinary build the check is the constant true.
+#ifdef MOE_CHECKED
+static __device__ int g_moe_bounds_prints;
+MOE_DEVICE bool moe_in_bounds(int site, int64_t index, int64_t limit, int32_t* status) {
+  if (index >= 0 && index < limit) return true;
+  set_status(status, MOE_DEV_ERR_BOUNDS);
+  if (atomicAdd(&g_moe_bounds_prints, 1) < 16)
+    printf("moe bounds check %d failed: index %lld, limit %lld (block %d, thread %d)\n", site, (long long)index,
+           (long long)limit, (int)blockIdx.x, (int)threadIdx.x);
+  return false;
+}
+#define MOE_IN_BOUNDS(site, index, limit, status) \
+  ::moe::moe_in_bounds((site), (int64_t)(index), (int64_t)(limit), (status))
+#else
+#define MOE_IN_BOUNDS(site, index, limit, status) true
+#endif
 
 MOE_DEVICE unsigned lanemask_lt() {
   unsigned m;

@@ -42,6 +42,7 @@ struct DispatchParams {
   int64_t scale_bytes;  // bytes of one output scale row
   int64_t nchunks;      // work items per token (row chunks)
   int64_t chunk_steps;  // loop steps of the row per chunk
+  int32_t* status;      // handle status word (bounds-checked builds report there)
 };
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -64,7 +65,8 @@ __device__ __forceinline__ void load_dests(const DispatchParams& p, const int32_
                                            int32_t* sdest, bool write_probs) {
   const int lane = threadIdx.x & 31;
   for (int k = lane; k < p.K; k += 32) {
-    const int32_t d = p.row_of[t * p.K + k];
+    int32_t d = p.row_of[t * p.K + k];
+    if (d >= 0 && !MOE_IN_BOUNDS(1, d, p.cap, p.status)) d = -1;
     sdest[k] = d;
     if (write_probs && d >= 0 && p.out_probs && p.probs) {
       float pr;
@@ -84,6 +86,7 @@ __device__ __forceinline__ void zero_pads(const DispatchParams& p, const int32_t
   const int64_t beg = (int64_t)soff[e] + p.counts[e];
   const int64_t end = min64(soff[e + 1], p.cap);
   const uint4 z = make_uint4(0, 0, 0, 0);
+  if (beg < end && !MOE_IN_BOUNDS(2, beg, p.cap, p.status)) return;
   for (int64_t r = beg; r < end; r++) {
     uint8_t* row = p.out + r * p.row_bytes;
     for (int64_t v = lane; v < p.row_bytes / 16; v += 32) st_vec(row + v * 16, z);
@@ -269,6 +272,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_nvfp4_kernel(DispatchParams
       for (int k = 0; k < p.K; k++) {
         const int32_t d = s_dest[warp][k];
         if (d < 0 || !live) continue;
+        if (!MOE_IN_BOUNDS(3, e0 + 8, H + 1, p.status)) continue;
         *reinterpret_cast<uint32_t*>(p.out + (int64_t)d * (H / 2) + e0 / 2) = packed;
         if ((lane & 1) == 0) p.out_scales[(int64_t)d * (H / 16) + e0 / 16] = (uint8_t)scode;
       }
@@ -667,6 +671,7 @@ cudaError_t launch_dispatch(const moe_handle_dev& h, const moe_shape& s, const m
   p.out = static_cast<uint8_t*>(out_tokens);
   p.out_probs = out_probs;
   p.out_scales = static_cast<uint8_t*>(out_scales);
+  p.status = h.status;
   const size_t smem = (size_t)(s.E + 1) * 4;
   // one warp per (token, row chunk) work item, plus one per expert for its pad rows
   switch (in_dtype) {

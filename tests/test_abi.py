@@ -162,6 +162,14 @@ def test_validation_rejects_before_any_launch(moe):
     assert lib.moe_grouped_mlp(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16, fake, None,
                                fake, None, fake, None, None, fake, 8, fake,
                                None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    # NVFP4 stages 256 K elements: I = 128 (valid for bf16 and FP8) is not built for it
+    glob = moe._Nvfp4Globals(fake, fake, fake, fake)
+    assert lib.moe_grouped_mlp(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_NVFP4, fake, fake,
+                               fake, fake, fake, fake, byref(glob), fake, 1 << 30, fake,
+                               None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_grouped_mlp(byref(handle), byref(moe._Shape(64, 384, 8, 2, 256)), byref(good_layout),
+                               moe.DTYPE_NVFP4, fake, fake, fake, fake, fake, fake, byref(glob), fake, 1 << 30,
+                               fake, None) == moe.MOE_ERR_UNSUPPORTED
     # extended grouped MLP: misaligned FC2 row probabilities, unknown output format, MX output without scales
     assert lib.moe_grouped_mlp_ex(byref(handle), byref(good_shape), byref(good_layout), moe.DTYPE_BF16, fake, None,
                                   fake, None, fake, None, None, fake, 1 << 30, moe.COMBINE_BF16, fake, None,

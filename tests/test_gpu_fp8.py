@@ -72,6 +72,8 @@ def _oracle_rows(oracle, w, r, rows, pre):
     ("small", _case(T=256, H=512, E=8, K=2, I=256)),
     ("ragged_h384", _case(T=300, H=384, E=6, K=3, I=128)),
     ("skewed_e32", _case(T=1024, H=256, E=32, K=4, I=384)),
+    ("max_experts_1024", _case(T=600, H=256, E=1024, K=2, I=128, m=8)),
+    ("one_expert", _case(T=300, H=256, E=1, K=1, I=128)),
 ], ids=lambda v: v if isinstance(v, str) else "")
 def test_fp8_layer_all_rows(oracle, moe, name, w):
     r = run_layer_fp8(moe, w, seed=61)

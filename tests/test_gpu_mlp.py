@@ -219,11 +219,11 @@ def test_whole_layer_in_one_cuda_graph(oracle, moe):
         assert layer_rel_err(oracle.bf16_to_f64(bits(out)), oracle.bf16_to_f64(ref), o_rows, wts) <= TOL_BF16
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "nvfp4"])
 def test_zero_token_layer(moe, dtype):
     """T = 0: all four calls run (the grouped MLP claims no tiles), the status
     word stays clear and nothing is written."""
-    w = _case("tiny", T=0, H=256, E=8, K=2, I=128)
+    w = _case("tiny", T=0, H=256, E=8, K=2, I=256 if dtype == "nvfp4" else 128)
     cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
     fmt, rmap, probs = workloads.routing_inputs(w, seed=1)
     shape, layout, routing_t, handle, _ = preprocess(moe, w, fmt, rmap, probs, cap)
@@ -233,6 +233,23 @@ def test_zero_token_layer(moe, dtype):
         y = fill_pattern(torch.empty(rows, w.H, dtype=torch.bfloat16, device="cuda"))
         ys = None
         wd, w13_s, w2_s, in_dtype = moe.DTYPE_BF16, None, None, moe.DTYPE_BF16
+        x = torch.empty(1, w.H, dtype=torch.bfloat16, device="cuda")
+    elif dtype == "nvfp4":
+        w13b, w2b = workloads.expert_weights(w, 1, device="cuda")
+        g13 = (w13b.float().abs().amax(dim=(1, 2)) / 2688.0).contiguous()
+        g2 = (w2b.float().abs().amax(dim=(1, 2)) / 2688.0).contiguous()
+        w13 = torch.empty(w.E, 2 * w.I, w.H // 2, dtype=torch.uint8, device="cuda")
+        w13_s = torch.empty(w.E, 2 * w.I, w.H // 16, dtype=torch.uint8, device="cuda")
+        w2 = torch.empty(w.E, w.H, w.I // 2, dtype=torch.uint8, device="cuda")
+        w2_s = torch.empty(w.E, w.H, w.I // 16, dtype=torch.uint8, device="cuda")
+        for e in range(w.E):
+            moe.moe_quantize_nvfp4_rows(w13b[e], g13[e:e + 1], w13[e], w13_s[e])
+            moe.moe_quantize_nvfp4_rows(w2b[e], g2[e:e + 1], w2[e], w2_s[e])
+        one = torch.ones(1, dtype=torch.float32, device="cuda")
+        glob = moe.Nvfp4Globals(one, one, g13, g2)
+        y = fill_pattern(torch.empty(rows, w.H // 2, dtype=torch.uint8, device="cuda"))
+        ys = torch.empty(rows, w.H // 16, dtype=torch.uint8, device="cuda")
+        wd, in_dtype = moe.DTYPE_NVFP4, moe.DTYPE_BF16_TO_NVFP4
         x = torch.empty(1, w.H, dtype=torch.bfloat16, device="cuda")
     else:
         w13b, w2b = workloads.expert_weights(w, 1, device="cuda")
@@ -247,12 +264,14 @@ def test_zero_token_layer(moe, dtype):
         wd, in_dtype = moe.DTYPE_FP8_E4M3_B128, moe.DTYPE_BF16_TO_FP8
         x = torch.empty(1, w.H, dtype=torch.bfloat16, device="cuda")
     yp = torch.empty(rows, dtype=torch.float32, device="cuda")
-    moe.moe_dispatch_permute(handle, shape, layout, in_dtype, x, None, routing_t, y, yp, ys)
+    moe.moe_dispatch_permute(handle, shape, layout, in_dtype, x, one if dtype == "nvfp4" else None, routing_t, y,
+                             yp, ys)
     ws = torch.empty(max(moe.moe_grouped_mlp_workspace_size(shape, layout, wd), 256), dtype=torch.uint8,
                      device="cuda")
     o = fill_pattern(torch.empty(rows, w.H, dtype=torch.bfloat16, device="cuda"))
     before = bits(o).copy()
-    moe.moe_grouped_mlp(handle, shape, layout, wd, y, ys, w13, w13_s, w2, w2_s, None, ws, o)
+    moe.moe_grouped_mlp(handle, shape, layout, wd, y, ys, w13, w13_s, w2, w2_s, glob if dtype == "nvfp4" else None,
+                        ws, o)
     out = fill_pattern(torch.empty(1, w.H, dtype=torch.bfloat16, device="cuda"))
     moe.moe_combine_unpermute(handle, shape, layout, o, yp, out)
     torch.cuda.synchronize()

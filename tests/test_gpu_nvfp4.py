@@ -109,6 +109,7 @@ def _check(oracle, w, r, toks):
     ("small", _case(T=64, H=512, E=8, K=2, I=256)),
     ("many_token_tiles", _case(T=512, H=256, E=4, K=2, I=256)),
     ("pad8_ragged", _case(T=77, H=512, E=6, K=3, I=512, m=8)),
+    ("one_expert", _case(T=40, H=256, E=1, K=1, I=256)),
 ], ids=lambda v: v if isinstance(v, str) else "")
 def test_nvfp4_layer_all_tokens(oracle, moe, name, w):
     r = run_layer_nvfp4(moe, w, seed=71)
