@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_f16_f32(BMW, BNT);
       const uint32_t smem_base = smem_u32(smem);
       int xs = 0, ast = 0, acc = 0;
-      uint32_t aphase = 0, xphase = 0, acc_phase = 0;
+      uint32_t aphase = 0, acc_phase = 0;
       const uint32_t xbase = smem_base + (uint32_t)kStages * kStageStride;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -397,10 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ast = 0;
             aphase ^= 1;
           }
-          if (++xs == kXSlots) {
-            xs = 0;
-            xphase ^= 1;
-          }
+          if (++xs == kXSlots) xs = 0;
         }
         if (!ok) break;
         if (lead) mma_commit(&s_tfull[acc]);
@@ -414,25 +411,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&s_drain);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&s_drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-        }
-      }
-      if (ok && lane == 0) {
-        // the releases of the last weight stages and token slots are mbarrier
-        // arrivals made when their MMAs complete: all of them land on this
-        // CTA's barriers before it leaves (the same waits a next stage would make)
-        for (int i = 0; i < kAStages && ok; i++) {
-          ok = mbar_wait(&s_aempty[ast], aphase ^ 1, abort_flag, p.status);
-          if (++ast == kAStages) {
-            ast = 0;
-            aphase ^= 1;
-          }
-        }
-        for (int i = 0; i < kXSlots && ok; i++) {
-          ok = mbar_wait(&s_xfree[xs], xphase ^ 1, abort_flag, p.status);
-          if (++xs == kXSlots) {
-            xs = 0;
-            xphase ^= 1;
-          }
         }
       }
     }
