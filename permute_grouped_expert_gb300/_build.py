@@ -59,6 +59,10 @@ def up_to_date(extra_flags=()) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    # MOE_CHECKED=1 in the environment selects the bounds-checked build for
+    # every caller (the tests, the bench) that builds with default flags
+    if not extra_flags and os.environ.get("MOE_CHECKED") == "1":
+        extra_flags = ("-DMOE_CHECKED",)
     if not force and up_to_date(extra_flags):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
