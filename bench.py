@@ -599,7 +599,8 @@ def run_ours(args, w):
         dom = "dispatch_permute"
         achieved = prob.dispatch_bytes(R) / (t_dis * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": profiled_traffic(w.name, "permute_grouped_expert_gb300/csrc/permute.cu"),
                 "peak_source": f"{peak_src} hbm_gbs"}
     else:
         peak = peaks["bf16_tflops"] * (2.0 if w.dtype == "fp8" else 4.0 if w.dtype == "nvfp4" else 1.0)
