@@ -106,9 +106,15 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return self.summarize(self.lines)
+
+    @staticmethod
+    def summarize(lines):
+        """Median SM clock and power, the highest max clock and the throttle
+        reasons seen Active, from nvidia-smi CSV lines of QUERY."""
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -136,7 +142,7 @@ def pre_roll_count(step_ms: float, minimum: int) -> int:
     """Warm replays that keep the GPU busy for PRE_ROLL_S after the clock sampler
     starts (its first sample comes 0.1-0.2 s later), so that the samples fall
     under load; at least `minimum`."""
-    return max(minimum, int(math.ceil(PRE_ROLL_S * 1e3 / max(step_ms, 1e-3))))
+    return max(minimum, int(math.ceil(PRE_ROLL_S * 1e3 / max(step_ms, 0.02))))
 
 
 # ------------------------------------------------------- multi-rank timing

@@ -35,3 +35,31 @@ def test_committed_summary_parses():
     path = os.path.join(bench.ROOT, "profiles", "grouped_mlp_bf16_fused_mid.md")
     text = open(path).read()
     assert "```roofline-traffic" in text and "traffic_bytes_per_launch:" in text
+
+
+def test_clock_samples_summary():
+    """Median clock and power under load, and every throttle reason seen Active."""
+    lines = [
+        "0, 2070, 2070, 512.30, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1995, 2070, 1390.10, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2010, 2070, 1388.70, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+        "0, [N/A], 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    got = bench.ClockSampler.summarize(lines)
+    assert got["sm_mhz"] == 2010.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"] and got["samples"] == 3
+    assert got["power_w"] == 1388.7
+
+
+def test_clock_samples_summary_reports_slowdown_reasons():
+    lines = ["0, 1500, 2070, 900.0, 0x8, Active, Not Active, Active, Not Active"]
+    got = bench.ClockSampler.summarize(lines)
+    assert got["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_pre_roll_keeps_the_gpu_busy_for_the_sampler():
+    # half a second of 4 ms steps, never fewer than the warm-up count
+    assert bench.pre_roll_count(4.0, 5) == 125
+    assert bench.pre_roll_count(1000.0, 5) == 5
+    assert bench.pre_roll_count(0.0, 3) == 25000  # a step timed at zero counts as 20 us
