@@ -49,6 +49,7 @@ COMBINE_MXFP4 = 2
 DEV_ERR_BAD_EXPERT = 1
 DEV_ERR_TOO_MANY_ROUTES = 2
 DEV_ERR_TIMEOUT = 4
+DEV_ERR_BOUNDS = 8  # bounds-checked builds only
 
 
 class _Shape(ctypes.Structure):

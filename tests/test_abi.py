@@ -41,6 +41,23 @@ def test_library_exports_every_declared_symbol(moe):
     assert set(names) == set(moe.exported_symbols())
 
 
+def test_binding_constants_match_the_header(moe):
+    """The Python binding's status, dtype and format constants equal the header's."""
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    defines = dict((k, int(v)) for k, v in re.findall(r"#define\s+MOE_(DEV_ERR_\w+)\s+(\d+)", text))
+    assert defines, "no device status bits found in moe.h"
+    for k, v in defines.items():
+        assert getattr(moe, k) == v, k
+    enums = dict((k, int(v)) for k, v in re.findall(r"\b(MOE_(?:ERR|OK|DTYPE|COMBINE|ROUTING)\w*)\s*=\s*(\d+)", text))
+    checked = 0
+    for k, v in enums.items():
+        name = k[4:] if k.startswith("MOE_DTYPE") or k.startswith("MOE_COMBINE") or k.startswith("MOE_ROUTING") else k
+        if hasattr(moe, name):
+            assert getattr(moe, name) == v, name
+            checked += 1
+    assert checked == len(enums), (checked, len(enums))
+
+
 def test_capacity_rule_golden(moe):
     path = os.path.join(ROOT, "tests", "golden", "capacity.txt")
     for line in open(path):
