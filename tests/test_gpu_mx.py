@@ -75,9 +75,9 @@ def test_combine_from_mx_rows(oracle, moe, elem, routing):
     assert np.all(np.abs(got - ref) <= bf16_ulp(ref))
 
 
-def _run_fp8_layer_mx(moe, w, seed, elem):
+def _run_fp8_layer_mx(moe, w, seed, elem, cap=None):
     fmt, rmap, probs = workloads.routing_inputs(w, seed)
-    cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m)
+    cap = workloads.unbounded_capacity(w.T, w.K, w.E, w.m) if cap is None else cap
     x = workloads.activations(w, seed)
     w13, w2 = workloads.expert_weights(w, seed, device="cuda")
     q13 = torch.empty(w13.shape, dtype=torch.uint8, device="cuda")
@@ -151,6 +151,31 @@ def test_fp8_layer_with_mx_fc2_output(oracle, moe, elem):
     w = workloads.scaled(workloads.WORKLOADS["dsv3"], T=256, H=512, E=8, K=2, I=256)
     r = _run_fp8_layer_mx(moe, w, 61, elem)
     _check_fp8_layer_mx(oracle, w, r, elem, np.arange(w.T))
+
+
+@pytest.mark.parametrize("elem", [0, 1])
+def test_fp8_layer_mx_output_ragged_hidden(oracle, moe, elem):
+    """H = 384: FC2's last 256-column tile is half past the rows' end; its second
+    half is computed but neither codes nor scales are written."""
+    w = workloads.scaled(workloads.WORKLOADS["dsv3"], T=200, H=384, E=6, K=3, I=256)
+    r = _run_fp8_layer_mx(moe, w, 62, elem)
+    _check_fp8_layer_mx(oracle, w, r, elem, np.arange(w.T))
+
+
+@pytest.mark.parametrize("elem", [0, 1])
+def test_fp8_layer_mx_output_capacity_cut(oracle, moe, elem):
+    """A capacity below the padded total: kept rows match the oracle, rows from
+    the capacity on are never written (their 0xFF pre-fill stays), and the
+    combine skips the dropped routes."""
+    w = workloads.scaled(workloads.WORKLOADS["dsv3"], T=256, H=512, E=8, K=2, I=256)
+    fmt, rmap, _ = workloads.routing_inputs(w, 63)
+    total = oracle.preprocess(fmt, rmap, w.T, w.E, w.K, w.m, 1 << 30)["total_rows"]
+    cap = int(total * 0.7) // 4 * 4
+    r = _run_fp8_layer_mx(moe, w, 63, elem, cap=cap)
+    pre = oracle.preprocess(r["fmt"], r["rmap"], w.T, w.E, w.K, w.m, cap)
+    assert pre["overflow"] == 1
+    _check_fp8_layer_mx(oracle, w, r, elem, np.arange(w.T))
+    assert np.all(r["oc"][pre["valid_rows"]:] == 0xFF) and np.all(r["osc"][pre["valid_rows"]:] == 0xFF)
 
 
 def test_dsv3_layer_with_mxfp8_combine_full_size_sampled(oracle, moe):
