@@ -50,6 +50,8 @@ CASES = [
     ("h1152_sparse", workloads.scaled(workloads.WORKLOADS["mid"], T=257, H=1152, E=16, K=4), "sparse", None),
     ("h2048_overflow", workloads.scaled(workloads.WORKLOADS["mid"], T=300, H=2048, E=16, K=8), "sparse", 0.7),
     ("h2176", workloads.scaled(workloads.WORKLOADS["permute"], T=130, H=2176, E=8, K=3), "dense", None),
+    # the largest top-k the API takes: four 32-route passes of the token kernel
+    ("h256_top128", workloads.scaled(workloads.WORKLOADS["stress"], T=150, H=256, E=256, K=128), "dense", None),
 ]
 
 

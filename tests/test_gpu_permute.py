@@ -37,6 +37,8 @@ PRE_CASES = [
     ("max_experts", _case("stress", T=3000, E=1024, K=8), None, None),
     ("ragged_tiles", _case("stress", T=4099, K=36), "sparse", None),
     ("zero_tokens", _case("tiny", T=0), None, None),
+    ("max_topk_128", _case("stress", T=300, E=256, K=128), "dense", None),
+    ("max_topk_128_sparse", _case("stress", T=300, E=256, K=128), "sparse", None),
 ]
 
 
@@ -118,6 +120,7 @@ def _dispatch(moe, w, fmt, rmap, probs, cap, x, in_dtype=None, x_scales=None, nv
     ("permute", _case("permute", T=2048), None),
     ("k36_sparse", _case("stress", T=1500, H=256), "sparse"),
     ("zero_tokens", _case("tiny", T=0), None),
+    ("max_topk_128", _case("stress", T=200, H=256, E=256, K=128), None),
 ], ids=lambda v: v if isinstance(v, str) else "")
 def test_dispatch_bf16_bitwise(oracle, moe, name, w, routing):
     fmt, rmap, probs = workloads.routing_inputs(w, seed=5, routing=routing)
@@ -255,6 +258,7 @@ def _combine(moe, handle, shape, layout, o, perm_probs, T, H):
     ("mid_sparse", _case("mid"), None, True),
     ("k36_sparse", _case("stress", T=700, H=512), "sparse", True),
     ("no_probs", _case("tiny", T=300), None, False),
+    ("max_topk_128", _case("stress", T=200, H=256, E=256, K=128), None, True),
 ], ids=lambda v: v if isinstance(v, str) else "")
 def test_combine_random_expert_rows(oracle, moe, name, w, routing, use_probs):
     fmt, rmap, probs = workloads.routing_inputs(w, seed=6, routing=routing)
