@@ -110,6 +110,30 @@ def _c_call(moe, fn, *args):
     return getattr(moe.library(), fn)(*args)
 
 
+def test_shape_and_layout_limits(moe):
+    """The documented limits of moe_shape / moe_layout are enforced before any
+    launch: 1 <= E <= 1024, 1 <= K <= min(E, 128), T >= 0, T*K and the padded
+    total below 2^31, capacity below 2^31, pad multiple >= 1."""
+    fake = ctypes.c_void_p(0x1000)
+    routing = moe._Routing(0, fake, None)
+    handle = moe._HandleDev(*([fake] * 8))
+    lib = moe.library()
+    byref = ctypes.byref
+
+    def pre(shape, layout):
+        return lib.moe_preprocess(byref(routing), byref(shape), byref(layout), byref(handle), fake, 1 << 40, None)
+
+    ok_layout = moe._Layout(32, 1024)
+    bad_shapes = [moe._Shape(64, 256, 0, 1, 0), moe._Shape(64, 256, 1025, 8, 0), moe._Shape(64, 256, 256, 129, 0),
+                  moe._Shape(64, 256, 4, 8, 0), moe._Shape(-1, 256, 8, 2, 0), moe._Shape(1 << 26, 256, 256, 32, 0),
+                  moe._Shape(64, 256, 8, 0, 0)]
+    for sh in bad_shapes:
+        assert pre(sh, ok_layout) == moe.MOE_ERR_INVALID_ARG, (sh.T, sh.E, sh.K)
+    good = moe._Shape(64, 256, 8, 2, 0)
+    for lay in [moe._Layout(0, 1024), moe._Layout(32, -1), moe._Layout(32, 1 << 31), moe._Layout(1 << 28, 1024)]:
+        assert pre(good, lay) == moe.MOE_ERR_INVALID_ARG, (lay.pad_multiple, lay.capacity)
+
+
 def test_validation_rejects_before_any_launch(moe):
     """Bad arguments return MOE_ERR_INVALID_ARG without touching the GPU
     (these pointers are never dereferenced)."""
